@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q4_0 weight-only matmul on GB300.
+
+Default workload (``--workload decode``): one decode step = the four 27B-class
+layer matrices (QKV 7168x5120, O 5120x5120, gate+up 34816x5120, down
+5120x17408) at M = 1, through q4_0_matmul.  Eight distinct layer copies
+(1.49 GB of Q4_0 weights, 11.6x the 129 MB L2) stay resident in HBM and step
+i uses copy i mod 8, so no step finds its weights in L2.  The metric is
+algorithmic GB/s (0.5625 N K + 2 M K + 4 M N bytes per matrix) with the
+weights-per-second equivalent in tokens/s of a 64-layer stack.
+
+Other workloads: ``batched`` (M = 16), ``prefill`` (M = 2048, TFLOP/s) and
+``sweep`` (64 layers at M = 1).  ``--impl reference`` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload).
+
+One JSON line is printed by rank 0.  Under torchrun every rank runs an
+independent replica (the matmul has no exchange step); the value is the
+bytes of all ranks over the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+SHAPE_ORDER = ("qkv", "o", "gate_up", "down")
+LAYER_WEIGHTS_64 = 21.139e9  # Q4_0 weights in 64 layers of the four matrices
+METRIC = "Q4_0 matmul: decode GB/s (% HBM peak), prefill TFLOP/s, tok/s-equivalent"
+
+
+def alg_bytes(M, N, K):
+    return 0.5625 * N * K + 2 * M * K + 4 * M * N
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["decode", "batched", "prefill", "sweep"], default="decode")
+    p.add_argument("--layers", type=int, default=8, help="resident layer copies (decode/batched)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=2000)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload_shapes(name):
+    from q4_0_weight_only_gb300 import synth
+    if name == "decode":
+        M = 1
+    elif name == "batched":
+        M = 16
+    elif name == "prefill":
+        M = 2048
+    else:
+        M = 1
+    return M, [(s, synth.SHAPES[s]) for s in SHAPE_ORDER]
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples of this process's GPU, 200 ms apart."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        import torch
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = str(device_index)
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+                except Exception:
+                    continue
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t0 - 1 <= r[0] <= self.t1 + 1] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3][1:5])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- our arm
+
+def build_layers(q4, synth, shapes, layers, device):
+    import torch
+    wq = []
+    for l in range(layers):
+        per = []
+        for s, (N, K) in shapes:
+            w = synth.device_layer_weights(l, s, device=device)
+            per.append(q4.quantize(w))
+            del w
+        wq.append(per)
+    torch.cuda.synchronize()
+    return wq
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from q4_0_weight_only_gb300 import build as lib_build
+    lib_build.build()
+    import q4_0_weight_only_gb300 as q4
+    from q4_0_weight_only_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    M, shapes = workload_shapes(args.workload)
+    layers = 64 if args.workload == "sweep" else (1 if args.workload == "prefill" else args.layers)
+    wq = build_layers(q4, synth, shapes, layers, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    xs = [torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16) for _, (N, K) in shapes]
+    ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _, (N, K) in shapes]
+    wss = [torch.empty(max(1, q4.lib().q4_0_matmul_workspace_bytes(M, N, K)), dtype=torch.uint8,
+                       device=dev) for _, (N, K) in shapes]
+    stream = torch.cuda.Stream(device=dev)
+
+    step_bytes = sum(alg_bytes(M, N, K) for _, (N, K) in shapes)
+    step_flops = sum(2.0 * M * N * K for _, (N, K) in shapes)
+    step_weights = sum(N * K for _, (N, K) in shapes)
+    sweep = args.workload == "sweep"
+
+    def enqueue_step(i):
+        ls = range(layers) if sweep else (i % layers,)
+        for l in ls:
+            for j, (_, (N, K)) in enumerate(shapes):
+                q4.matmul(xs[j], wq[l][j], N, K, out=ys[j], workspace=wss[j], stream=stream)
+
+    # one CUDA graph per step variant (layer copy), replayed step by step
+    graphs = []
+    with torch.cuda.stream(stream):
+        for i in range(3):  # load/initialise before capture
+            enqueue_step(i)
+        stream.synchronize()
+        for v in range(1 if sweep else layers):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                enqueue_step(v)
+            graphs.append(gr)
+    launches_per_step = 4 * (layers if sweep else 1)
+
+    warm = max(3, args.warmup)
+    for i in range(warm):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % len(graphs)].replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    clocks.mark_end()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_local = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms_local, world)
+    clk = clocks.stop()
+    if q4.device_error() != 0:
+        raise RuntimeError("a kernel reported a device timeout during the benchmark")
+
+    sec = ms / 1e3
+    gbs = step_bytes * args.steps * world / sec / 1e9
+    tflops = step_flops * args.steps * world / sec / 1e12
+    tok_s = M * step_weights * args.steps * world / sec / LAYER_WEIGHTS_64
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    x_host = [torch.empty((M, K), dtype=torch.bfloat16).pin_memory() for _, (N, K) in shapes]
+    for j, xh in enumerate(x_host):
+        xh.copy_(xs[j].cpu())
+    y_host = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _, (N, K) in shapes]
+    h2d = sum(x.numel() * 2 for x in x_host) * (layers if sweep else 1)
+    d2h = sum(y.numel() * 4 for y in y_host) * (layers if sweep else 1)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            ls = range(layers) if sweep else (i % layers,)
+            for l in ls:
+                for j, (_, (N, K)) in enumerate(shapes):
+                    xs[j].copy_(x_host[j], non_blocking=True)
+                    q4.matmul(xs[j], wq[l][j], N, K, out=ys[j], workspace=wss[j], stream=stream)
+                    y_host[j].copy_(ys[j], non_blocking=True)
+            stream.synchronize()
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+    e2e_val = (step_bytes if M < 256 else step_flops) * e2e_steps * world / t_e2e / (1e9 if M < 256 else 1e12)
+
+    unit = "GB/s" if M < 256 else "TFLOP/s"
+    value = gbs if M < 256 else tflops
+    # roofline of the dominant kernel (the only kernel in the timed region)
+    launches = args.steps * launches_per_step
+    if M < 256:
+        roof = {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(gbs / world / hbm, 4), "traffic": None,
+                "kernel": "gemv_kernel<1>" if M == 1 else "gemv_kernel", "peak_source": peak_kind,
+                "avg_launch_us": round(ms_local * 1e3 / launches, 3)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tflops / world, 1), "peak": tf_sust,
+                "unit": "TFLOP/s", "frac": round(tflops / world / tf_sust, 4), "traffic": None,
+                "kernel": "gemm_kernel<256>", "peak_source": peak_kind + " sustained",
+                "avg_launch_us": round(ms_local * 1e3 / launches, 3)}
+    traffic = load_traffic(args.workload)
+    if traffic is not None:
+        roof["traffic"] = traffic
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": warm, "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "q4_0 weights; f16 FMA in-block, f32 across blocks" if M < 256 else
+                 "q4_0 weights -> f16 tiles; f16 MMA, f32 accumulate",
+        "data": "synthetic: W ~ N(0, 0.02) quantized on device, x ~ N(0, 1) bf16",
+        "config": {"workload": workload_name(args.workload, M, layers), "M": M,
+                   "shapes": {s: list(nk) for s, nk in shapes}, "layer_copies": layers,
+                   "l2": "inputs larger than L2: %d resident layer copies, %.2f GB cycled"
+                         % (layers, layers * sum(0.5625 * N * K for _, (N, K) in shapes) / 1e9),
+                   "parallelism": f"replicas x{world}", "graph": "one CUDA graph per step"},
+        "tok_s_eq": round(tok_s, 1),
+        "tflops": round(tflops, 2),
+        "gpu_launches": launches,
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": {"value": round(e2e_val, 2), "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wq[0], xs, shapes, M, budget_s=10.0)
+    return line if rank == 0 else None
+
+
+def workload_name(w, M, layers):
+    return {"decode": f"decode M=1, four 27B-class layer matrices per step, {layers} layer copies",
+            "batched": f"batched decode M={M}, four 27B-class layer matrices per step",
+            "prefill": f"prefill M={M}, four 27B-class layer matrices per step",
+            "sweep": "64-layer decode sweep at M=1 (256 matrices per step)"}[w]
+
+
+def load_traffic(workload):
+    """dram bytes per launch from the committed ncu summary, if it covers the
+    current kernels (written by hand from an ncu capture; see profiles/)."""
+    path = os.path.join(HERE, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(workload)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def cpu_baseline(wq_layer, xs, shapes, M, budget_s=10.0):
+    """The oracle on the host cores over a bounded sample of the workload."""
+    import oracle
+    o = oracle.get()
+    host_w = [w.cpu().numpy() for w in wq_layer]
+    host_x = [x.view(__import__("torch").int16).cpu().numpy().view(np.uint16) for x in xs]
+    done_bytes, done_flops, t_used, reps = 0.0, 0.0, 0.0, 0
+    while t_used < budget_s:
+        for j, (_, (N, K)) in enumerate(shapes):
+            rows = N if M < 256 else max(1, N // 64)
+            t0 = time.perf_counter()
+            o.matmul(host_x[j][:M], host_w[j][:rows], rows, K)
+            t_used += time.perf_counter() - t0
+            done_bytes += alg_bytes(M, rows, K)
+            done_flops += 2.0 * M * rows * K
+        reps += 1
+    unit = "GB/s" if M < 256 else "TFLOP/s"
+    val = done_bytes / t_used / 1e9 if M < 256 else done_flops / t_used / 1e12
+    return {"value": round(val, 4), "unit": unit, "cores": o.threads(), "kind": "oracle",
+            "sample": f"{reps} pass(es) of the four matrices at M={M}"
+                      + ("" if M < 256 else " on 1/64 of the rows") + f", {t_used:.1f} s"}
+
+
+def run_reference(args, rank, world, local):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    workload (a slice of rows of each matrix) on the host cores."""
+    if rank != 0:
+        return None
+    import oracle
+    from q4_0_weight_only_gb300 import synth
+    o = oracle.get()
+    M, shapes = workload_shapes(args.workload)
+    warm = max(3, args.warmup)
+    total_steps = args.steps + warm
+    per_step_budget = min(0.5, 150.0 / total_steps)
+    # probe the oracle's speed on a small slice to size the per-step sample
+    rng = np.random.default_rng(0)
+    host = []
+    for s, (N, K) in shapes:
+        rows = min(N, 1024)
+        wq = o.quantize(synth.weights(synth.generator(100 + SHAPE_ORDER.index(s)), rows, K))
+        x = synth.to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+        host.append((N, K, wq, x))
+    t0 = time.perf_counter()
+    for N, K, wq, x in host:
+        o.matmul(x, wq[:64], 64, K)
+    per_row = (time.perf_counter() - t0) / (64 * len(host))
+    rows = int(max(1, min(1024, per_step_budget / max(per_row * len(host), 1e-9))))
+    for _ in range(warm):
+        for N, K, wq, x in host:
+            o.matmul(x, wq[:rows], rows, K)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for N, K, wq, x in host:
+            o.matmul(x, wq[:rows], rows, K)
+    t = time.perf_counter() - t0
+    byts = sum(alg_bytes(M, rows, K) for N, K, _, _ in host) * args.steps
+    flops = sum(2.0 * M * rows * K for N, K, _, _ in host) * args.steps
+    unit = "GB/s" if M < 256 else "TFLOP/s"
+    val = byts / t / 1e9 if M < 256 else flops / t / 1e12
+    sample = f"{rows} rows of each of the four matrices per step at M={M}"
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": warm,
+            "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(args.workload, M, 1), "M": M,
+                       "shapes": {s: list(nk) for s, nk in shapes}},
+            "cpu_baseline": {"value": round(val, 4), "unit": unit, "cores": o.threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 4), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world, local)
+    else:
+        line = run_ours(args, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * q4_0.h -- C ABI of libq4_0.so: matmul of bf16 activations with weights
+ * stored in Q4_0, on one NVIDIA GB300 (sm_103a).
+ *
+ * Operation.  "Vertical disaggregation: maximizing model throughput on
+ * heterogeneous silicon", section "Every cycle counts: custom kernels": the
+ * CPU and the GPU paths share one Q4_0 weight format, produce deterministic
+ * output, and are built from nibble unpack, dot product, scale apply, batch
+ * decode and a GPU "Q4_0 -> Tensor Core" path.  This library is that GPU
+ * path, written for sm_103a: a memory-bound GEMV for decode (small M) and a
+ * tcgen05 tensor-core GEMM for prefill (large M), behind one dispatcher.
+ *
+ * Q4_0 format (the layout this library fixes; the page prints none):
+ *   - a weight matrix W [N][K] is stored as N rows of K/32 blocks, row-major,
+ *     one row = 18*K/32 contiguous bytes;
+ *   - block = 18 bytes: bytes 0-1 an IEEE binary16 scale d (little-endian),
+ *     bytes 2-17 sixteen code bytes qs[16];
+ *   - element j (0..15) of the block is qs[j] & 15, element j+16 is qs[j] >> 4;
+ *   - weight value w = d * (q - 8).
+ *
+ * Conventions for every entry point below:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no pointer after the call returns and allocates nothing that
+ *     outlives a call.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued asynchronously on it; the caller synchronises.  Launch errors
+ *     are returned; a device-side timeout is recorded in a device error word
+ *     that q4_0_device_error() reads.
+ *   - Arguments are validated before anything is launched; an invalid call
+ *     returns a negative status and enqueues nothing.
+ *   - No entry point prints, exits, or keeps host-side mutable state; calls
+ *     from several host threads are safe.
+ *   - Results are deterministic: the same inputs give bit-identical outputs
+ *     (fixed reduction order, no floating-point atomics).
+ */
+#ifndef Q4_0_H_
+#define Q4_0_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q4_0_BLOCK_WEIGHTS 32
+#define Q4_0_BLOCK_BYTES 18
+#define Q4_0_VERSION 1
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    Q4_0_OK = 0,
+    Q4_0_ERR_INVALID_ARG = -1,    /* null pointer, bad size, misaligned pointer */
+    Q4_0_ERR_UNSUPPORTED = -2,    /* valid Q4_0 call outside what this build runs */
+    Q4_0_ERR_CUDA = -3,           /* a CUDA runtime call or a launch failed */
+    Q4_0_ERR_DEVICE_TIMEOUT = -4, /* a kernel gave up on a bounded wait */
+    Q4_0_ERR_WORKSPACE = -5       /* workspace missing or too small */
+} q4_0_status;
+
+/* Library version (Q4_0_VERSION). */
+int q4_0_version(void);
+
+/* Static text for a status code; never NULL. */
+const char *q4_0_status_string(int status);
+
+/* Bytes of a Q4_0 matrix of N rows and K columns: N * K/32 * 18.
+ * Returns 0 when N < 1, K < 1 or K is not a multiple of 32. */
+size_t q4_0_weight_bytes(int64_t N, int64_t K);
+
+/*
+ * q4_0_quantize -- fp32 weights -> Q4_0 blocks.
+ *   w   : float [N][K] row-major, device.  Values must be finite and
+ *         |w| <= 8 * 65504 (the scale must fit binary16).
+ *   wq  : uint8 [q4_0_weight_bytes(N, K)], device, written completely.
+ *   N, K: N >= 1, K >= 32, K % 32 == 0.
+ * Per block of 32 weights: d = (signed value of the max-|w| element, first
+ * index on ties) / -8 in fp32; the stored scale is d rounded to binary16
+ * (nearest, ties to even); each code is q = clamp(round(w / d) + 8, 0, 15)
+ * with the fp32 d, IEEE division and round-half-away-from-zero; an all-zero
+ * block stores d = +0 and codes 8.  Codes match the library's CPU reference
+ * bit for bit.
+ * Alignment: w 16 bytes; wq 2 bytes.
+ * Returns Q4_0_OK, Q4_0_ERR_INVALID_ARG or Q4_0_ERR_CUDA.
+ */
+int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *stream);
+
+/*
+ * q4_0_matmul -- y = x * W^T with W in Q4_0.
+ *   x   : bf16 bit patterns [M][K] row-major, device (the __nv_bfloat16 type).
+ *   wq  : Q4_0 matrix W [N][K] as above, device.
+ *   y   : float [M][N] row-major, device, fully overwritten (no accumulate).
+ *   M, N, K: M >= 1, N >= 1, K >= 256, K % 256 == 0 (K % 32 != 0 is
+ *         INVALID_ARG; K % 32 == 0 but K % 256 != 0 is UNSUPPORTED).
+ * y[m][n] = sum_k d(n,k) * (q(n,k) - 8) * x[m][k], accumulated in fp32.
+ * Dispatch: M <= 32 runs the decode GEMV (weights streamed once, fp32
+ * accumulation of per-block fp16 partial sums); M > 32 runs the tcgen05 GEMM
+ * (weights dequantised to binary16 tiles, x rounded to binary16, fp32
+ * accumulation in tensor memory).  Both meet: per element
+ * |y - y_exact| <= 1e-2 * sum_k |w x| and relative L2 error <= 2e-3.
+ * Activations must be finite with |x| <= 65504 (the GEMM rounds x to
+ * binary16).
+ * Scratch: the GEMM path needs q4_0_matmul_workspace_bytes(M, N, K) bytes;
+ * this entry point takes them with cudaMallocAsync on `stream` and frees
+ * them with cudaFreeAsync on the same stream.  Use q4_0_matmul_ws to supply
+ * the workspace yourself.
+ * Alignment: x, wq and y 16 bytes.
+ * Returns Q4_0_OK, Q4_0_ERR_INVALID_ARG, Q4_0_ERR_UNSUPPORTED or Q4_0_ERR_CUDA.
+ */
+int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y,
+                int64_t M, int64_t N, int64_t K, void *stream);
+
+/* Scratch bytes q4_0_matmul needs for these sizes (0 for the GEMV path). */
+size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * q4_0_matmul_ws -- q4_0_matmul with caller-owned scratch.
+ *   workspace       : device pointer, 256-byte aligned, at least
+ *                     q4_0_matmul_workspace_bytes(M, N, K) bytes (may be
+ *                     NULL when that is 0).  Contents on entry are ignored;
+ *                     it is in use until the work on `stream` completes.
+ *   workspace_bytes : its size.
+ * Returns Q4_0_ERR_WORKSPACE when the workspace is missing or too small,
+ * otherwise as q4_0_matmul.
+ */
+int q4_0_matmul_ws(const uint16_t *x, const uint8_t *wq, float *y,
+                   int64_t M, int64_t N, int64_t K,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q4_0_gemv -- the decode kernel alone (what q4_0_matmul runs for M <= 32).
+ * Same arguments, layout and result contract as q4_0_matmul; M <= 32
+ * (larger M is UNSUPPORTED).  Needs no workspace.
+ */
+int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y,
+              int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * q4_0_gemm -- the tcgen05 prefill kernel alone (what q4_0_matmul runs for
+ * M > 32), usable at any M >= 1 for cross-checks.  Workspace as in
+ * q4_0_matmul_ws (q4_0_gemm_workspace_bytes(M, K) bytes: x rounded to
+ * binary16).
+ */
+size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t K);
+int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y,
+              int64_t M, int64_t N, int64_t K,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q4_0_device_error -- read and clear the device error word of the current
+ * device.  Synchronises the device.  *code receives Q4_0_OK or
+ * Q4_0_ERR_DEVICE_TIMEOUT (a kernel gave up on a bounded wait and left its
+ * output incomplete).  Returns Q4_0_OK or Q4_0_ERR_CUDA.
+ */
+int q4_0_device_error(int *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4_0_H_ */

@@ -1,0 +1,13 @@
+"""Q4_0 weight-only matmul for one NVIDIA GB300 (sm_103a).
+
+The compute lives in libq4_0.so (hand-written CUDA: a decode GEMV, a tcgen05
+tensor-core GEMM and a quantizer); this package is its thin Python binding.
+Build it with ``q4_0_weight_only_gb300.build.build()``.
+"""
+from ._lib import (ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_INVALID_ARG, ERR_UNSUPPORTED,
+                   ERR_WORKSPACE, OK, Q4Error, device_error, gemm, gemv, lib, matmul,
+                   matmul_alloc, quantize, status_string, version, weight_bytes)
+
+__all__ = ["quantize", "matmul", "matmul_alloc", "gemv", "gemm", "weight_bytes", "device_error",
+           "version", "status_string", "lib", "Q4Error", "OK", "ERR_INVALID_ARG",
+           "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_DEVICE_TIMEOUT", "ERR_WORKSPACE"]

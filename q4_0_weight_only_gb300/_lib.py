@@ -1,0 +1,188 @@
+"""Python binding of libq4_0.so (argument marshalling only).
+
+Every function checks the tensors it is given (dtype, device, shape,
+contiguity), passes raw device pointers and the current CUDA stream to the
+C ABI declared in include/q4_0.h, and raises Q4Error on a non-zero status.
+All arithmetic happens in the library's CUDA kernels; there is no fallback:
+if the library is not built, the first call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libq4_0.so")
+
+# Status codes (include/q4_0.h).
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_CUDA = -3
+ERR_DEVICE_TIMEOUT = -4
+ERR_WORKSPACE = -5
+
+# Every entry point the header declares, with its ctypes signature.
+_P, _I64, _SZ, _INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+SIGNATURES = {
+    "q4_0_version": ([], _INT),
+    "q4_0_status_string": ([_INT], ctypes.c_char_p),
+    "q4_0_weight_bytes": ([_I64, _I64], _SZ),
+    "q4_0_quantize": ([_P, _P, _I64, _I64, _P], _INT),
+    "q4_0_matmul": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "q4_0_matmul_workspace_bytes": ([_I64, _I64, _I64], _SZ),
+    "q4_0_matmul_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
+    "q4_0_gemv": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "q4_0_gemm_workspace_bytes": ([_I64, _I64], _SZ),
+    "q4_0_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
+    "q4_0_device_error": ([ctypes.POINTER(_INT)], _INT),
+}
+
+_lib = None
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def lib():
+    """Load libq4_0.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with q4_0_weight_only_gb300.build.build() "
+                "(nvcc, sm_103a). There is no fallback implementation.")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().q4_0_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise Q4Error(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def version() -> int:
+    return int(lib().q4_0_version())
+
+
+def weight_bytes(N: int, K: int) -> int:
+    return int(lib().q4_0_weight_bytes(N, K))
+
+
+def quantize(w: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """fp32 [N, K] -> Q4_0 bytes uint8 [N, K/32*18] (device)."""
+    _need(w, "w", torch.float32, 2)
+    N, K = w.shape
+    nbytes = weight_bytes(N, K)
+    if nbytes == 0:
+        raise ValueError("K must be a positive multiple of 32")
+    if out is None:
+        out = torch.empty((N, nbytes // N), dtype=torch.uint8, device=w.device)
+    _need(out, "out", torch.uint8, 2)
+    if out.numel() != nbytes:
+        raise ValueError("out has the wrong size")
+    _check(lib().q4_0_quantize(w.data_ptr(), out.data_ptr(), N, K, _stream(stream)), "q4_0_quantize")
+    return out
+
+
+def _mm_args(x, wq, N, K, out):
+    _need(x, "x", torch.bfloat16, 2)
+    _need(wq, "wq", torch.uint8, 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] must equal K")
+    if wq.numel() != weight_bytes(N, K):
+        raise ValueError("wq does not hold an N x K Q4_0 matrix")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _need(out, "out", torch.float32, 2)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N]")
+    return M, out
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() < nbytes:
+        raise ValueError("workspace too small")
+    return workspace, workspace.numel()
+
+
+def matmul(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
+           workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """y = x W^T: x bf16 [M, K], wq Q4_0 [N, K] -> fp32 [M, N] (the dispatcher)."""
+    M, out = _mm_args(x, wq, N, K, out)
+    ws, wsb = _workspace(int(lib().q4_0_matmul_workspace_bytes(M, N, K)), x.device, workspace)
+    _check(lib().q4_0_matmul_ws(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
+                                ws.data_ptr() if ws is not None else None, wsb, _stream(stream)),
+           "q4_0_matmul")
+    return out
+
+
+def matmul_alloc(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
+                 stream=None) -> torch.Tensor:
+    """Same as matmul, through q4_0_matmul (the library takes its own scratch)."""
+    M, out = _mm_args(x, wq, N, K, out)
+    _check(lib().q4_0_matmul(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)),
+           "q4_0_matmul")
+    return out
+
+
+def gemv(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
+         stream=None) -> torch.Tensor:
+    """The decode kernel alone (M <= 32)."""
+    M, out = _mm_args(x, wq, N, K, out)
+    _check(lib().q4_0_gemv(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)),
+           "q4_0_gemv")
+    return out
+
+
+def gemm(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
+         workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """The tcgen05 kernel alone (any M)."""
+    M, out = _mm_args(x, wq, N, K, out)
+    ws, wsb = _workspace(int(lib().q4_0_gemm_workspace_bytes(M, K)), x.device, workspace)
+    _check(lib().q4_0_gemm(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
+                           ws.data_ptr(), wsb, _stream(stream)), "q4_0_gemm")
+    return out
+
+
+def device_error() -> int:
+    """Read and clear the device error word (synchronises the device)."""
+    code = ctypes.c_int(0)
+    _check(lib().q4_0_device_error(ctypes.byref(code)), "q4_0_device_error")
+    return code.value

@@ -1,0 +1,194 @@
+// api.cu -- the C ABI of libq4_0.so (declared in include/q4_0.h): argument
+// validation, the M-based dispatch between the decode GEMV and the tcgen05
+// GEMM, scratch handling and the device error word.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/q4_0.h"
+#include "q4_0_internal.h"
+
+namespace q4_0 {
+
+// Written by a kernel that abandons a bounded wait; read and cleared by
+// q4_0_device_error().
+__device__ unsigned int g_device_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<unsigned int *> g_err_ptr[kMaxDevices];
+}  // namespace
+
+int device_sm_count(int device) {
+    if (device < 0 || device >= kMaxDevices) return 0;
+    int v = g_sm_count[device].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+    g_sm_count[device].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+cudaError_t ensure_smem_attr(const void *func, int bytes) {
+    struct Entry {
+        const void *func;
+        int device;
+        int bytes;
+    };
+    static std::mutex mu;
+    static Entry done[256];
+    static int ndone = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ndone; ++i)
+        if (done[i].func == func && done[i].device == dev && done[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < ndone; ++i)
+        if (done[i].func == func && done[i].device == dev) {
+            done[i].bytes = bytes;
+            return cudaSuccess;
+        }
+    if (ndone < 256) done[ndone++] = Entry{func, dev, bytes};
+    return cudaSuccess;
+}
+
+unsigned int *device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned int *p = g_err_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_error_word) != cudaSuccess) return nullptr;
+    p = static_cast<unsigned int *>(addr);
+    g_err_ptr[dev].store(p, std::memory_order_release);
+    return p;
+}
+
+}  // namespace q4_0
+
+using namespace q4_0;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Common validation of a matmul call.
+int check_matmul_args(const void *x, const void *wq, const void *y, int64_t M, int64_t N,
+                      int64_t K) {
+    if (!x || !wq || !y) return Q4_0_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return Q4_0_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(wq) || !aligned16(y)) return Q4_0_ERR_INVALID_ARG;
+    if (K % 256 != 0) return Q4_0_ERR_UNSUPPORTED;
+    // keep every index and TMA coordinate in 32-bit range
+    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 24)) return Q4_0_ERR_UNSUPPORTED;
+    if (M * K > (1ll << 40) || N * K > (1ll << 40) || M * N > (1ll << 40))
+        return Q4_0_ERR_UNSUPPORTED;
+    return Q4_0_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? Q4_0_OK : Q4_0_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int q4_0_version(void) { return Q4_0_VERSION; }
+
+const char *q4_0_status_string(int status) {
+    switch (status) {
+        case Q4_0_OK: return "ok";
+        case Q4_0_ERR_INVALID_ARG: return "invalid argument";
+        case Q4_0_ERR_UNSUPPORTED: return "unsupported by this build";
+        case Q4_0_ERR_CUDA: return "CUDA error";
+        case Q4_0_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case Q4_0_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+size_t q4_0_weight_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 1 || K % 32 != 0) return 0;
+    return (size_t)N * (size_t)(K / 32) * Q4_0_BLOCK_BYTES;
+}
+
+int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *stream) {
+    if (!w || !wq || N < 1 || K < 32 || K % 32 != 0) return Q4_0_ERR_INVALID_ARG;
+    if (!aligned16(w) || (reinterpret_cast<uintptr_t>(wq) & 1u)) return Q4_0_ERR_INVALID_ARG;
+    if (N * (K / 32) > (1ll << 40)) return Q4_0_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize(w, wq, N, K, static_cast<cudaStream_t>(stream),
+                                     device_error_word()));
+}
+
+size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t K) {
+    if (M < 1 || K < 1) return 0;
+    return gemm_workspace_bytes(M, K);
+}
+
+size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    if (M <= 32) return 0;
+    return q4_0_gemm_workspace_bytes(M, K);
+}
+
+int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+              void *stream) {
+    int st = check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    if (M > 32) return Q4_0_ERR_UNSUPPORTED;
+    unsigned int *err = device_error_word();
+    if (!err) return Q4_0_ERR_CUDA;
+    return from_cuda(launch_gemv(x, wq, y, M, N, K, static_cast<cudaStream_t>(stream), err));
+}
+
+int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+              void *workspace, size_t workspace_bytes, void *stream) {
+    int st = check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    if (!workspace || workspace_bytes < gemm_workspace_bytes(M, K) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return Q4_0_ERR_WORKSPACE;
+    unsigned int *err = device_error_word();
+    if (!err) return Q4_0_ERR_CUDA;
+    return from_cuda(launch_gemm(x, wq, y, M, N, K, workspace, static_cast<cudaStream_t>(stream), err));
+}
+
+int q4_0_matmul_ws(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    int st = check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    if (M <= 32) return q4_0_gemv(x, wq, y, M, N, K, stream);
+    return q4_0_gemm(x, wq, y, M, N, K, workspace, workspace_bytes, stream);
+}
+
+int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+                void *stream) {
+    int st = check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    if (M <= 32) return q4_0_gemv(x, wq, y, M, N, K, stream);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = gemm_workspace_bytes(M, K);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return Q4_0_ERR_CUDA;
+    st = q4_0_gemm(x, wq, y, M, N, K, ws, bytes, stream);
+    const cudaError_t fe = cudaFreeAsync(ws, s);
+    if (st == Q4_0_OK && fe != cudaSuccess) st = Q4_0_ERR_CUDA;
+    return st;
+}
+
+int q4_0_device_error(int *code) {
+    if (!code) return Q4_0_ERR_INVALID_ARG;
+    unsigned int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return Q4_0_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_device_error_word, sizeof v) != cudaSuccess) return Q4_0_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof zero) != cudaSuccess)
+        return Q4_0_ERR_CUDA;
+    *code = v ? Q4_0_ERR_DEVICE_TIMEOUT : Q4_0_OK;
+    return Q4_0_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,339 @@
+// gemm.cu -- prefill GEMM y = x * W^T on the 5th-generation tensor cores.
+//
+// "Vertical disaggregation: maximizing model throughput on heterogeneous
+// silicon", section "Every cycle counts: custom kernels" names a GPU
+// "Q4_0 -> Tensor Core" path over the shared Q4_0 format.  On sm_103a:
+//
+//   * x (bf16) is first rounded to binary16 into a scratch buffer, because a
+//     tcgen05 kind::f16 MMA takes A and B of one type and binary16 operand
+//     tiles keep the result well inside the error budget (bf16 weight tiles
+//     would not);
+//   * one CTA computes a 128 (weight rows) x TM (x rows) tile of y^T;
+//     warp 0 streams Q4_0 weight tiles [128 rows x 256 k] (144 bytes per row)
+//     and 128-byte-swizzled x tiles [TM rows x 64 k] with tensor TMA;
+//   * warps 2-5 (one thread per weight row) unpack nibbles, apply the scale
+//     in binary16 (d * (q - 8), one rounding) and store the tile into tensor
+//     memory with tcgen05.st -- the A operand of the MMA lives in TMEM, so
+//     dequantised weights never touch shared memory;
+//   * warp 1 issues tcgen05.mma (M = 128, N = TM, K = 16) with A from TMEM,
+//     B from shared memory, fp32 accumulation in TMEM;
+//   * warps 2-5 then read the accumulator with tcgen05.ld and store y with
+//     32 consecutive n per warp store (coalesced).
+// All pipeline waits are bounded (see q4_0_ptx.cuh); the reduction order is
+// fixed, so results are deterministic.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <mutex>
+
+#include "q4_0_internal.h"
+#include "q4_0_ptx.cuh"
+
+namespace q4_0 {
+namespace {
+
+constexpr int kTileN = 128;                 // weight rows per CTA (MMA M)
+constexpr int kKB = 64;                     // k per MMA stage
+constexpr int kKW = 256;                    // k per weight stage
+constexpr int kWRowBytes = kKW / 32 * 18;   // 144
+constexpr int kWStageBytes = kTileN * kWRowBytes;
+constexpr int kNW = 3, kNX = 4, kNA = 4;    // ring depths
+constexpr int kThreads = 192;
+
+__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
+    uint32_t p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+template <int TM>
+struct GemmCfg {
+    static constexpr uint32_t kXStage = TM * 128;
+    static constexpr uint32_t kDCols = TM < 32 ? 32 : TM;
+    static constexpr uint32_t kCols = pow2_at_least(kDCols + kNA * 32);
+    static constexpr size_t kBarOff = (size_t)kNX * kXStage + (size_t)kNW * kWStageBytes;
+    static constexpr int kNumBars = 2 * kNW + 2 * kNX + 2 * kNA + 2;
+    static constexpr size_t kSmem = 1024 + kBarOff + kNumBars * 8 + 16;
+};
+
+__device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
+__device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// bf16 -> binary16 (round to nearest even), 8 elements per thread.
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__ x,
+                                                       uint4 *__restrict__ x16, int64_t n8) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const uint4 u = __ldg(x + i);
+    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+        out[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16),
+                                       __uint_as_float(in[h] & 0xFFFF0000u)));
+    x16[i] = make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// One Q4_0 block -> 16 TMEM columns of packed binary16 pairs: column c
+// holds elements (2c, 2c + 1) of the block, each d * (q - 8) rounded once.
+__device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q)[4],
+                                              uint32_t *out) {
+    const uint32_t kMagic = 0x64006400u;
+    const half2 k1032 = __floats2half2_rn(1032.0f, 1032.0f);
+    const half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits));
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        const uint32_t b01 = __byte_perm(Q[wi], 0u, 0x4140);  // [qs0, 0, qs1, 0]
+        const uint32_t b23 = __byte_perm(Q[wi], 0u, 0x4342);  // [qs2, 0, qs3, 0]
+        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((b01 & 0x000F000Fu) | kMagic), k1032), d2));
+        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((b23 & 0x000F000Fu) | kMagic), k1032), d2));
+        out[8 + 2 * wi + 0] =
+            h2u(__hmul2(__hsub2(u2h(((b01 >> 4) & 0x000F000Fu) | kMagic), k1032), d2));
+        out[8 + 2 * wi + 1] =
+            h2u(__hmul2(__hsub2(u2h(((b23 >> 4) & 0x000F000Fu) | kMagic), k1032), d2));
+    }
+}
+
+template <int TM>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                float *__restrict__ y, int M, int N, int K, unsigned int *err) {
+    using Cfg = GemmCfg<TM>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *xring = smem;
+    uint8_t *wring = smem + kNX * Cfg::kXStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
+    uint64_t *w_full = bars, *w_empty = bars + kNW;
+    uint64_t *x_full = bars + 2 * kNW, *x_empty = x_full + kNX;
+    uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNA;
+    uint64_t *d_full = a_empty + kNA, *drain = d_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * TM;
+    const int KS = K / kKB, KWS = K / kKW;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNW; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&w_empty[i], 128);
+        }
+        for (int i = 0; i < kNX; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);
+        }
+        for (int i = 0; i < kNA; ++i) {
+            mbar_init(&a_full[i], 128);
+            mbar_init(&a_empty[i], 1);
+        }
+        mbar_init(d_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&wmap);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, Cfg::kCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t d_tmem = tmem;
+    const uint32_t a_tmem = tmem + Cfg::kDCols;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // producer: weight stage ws, then its four x stages
+            int issued_w = 0, issued_x = 0;
+            for (int ws = 0; ws < KWS; ++ws) {
+                const int wsl = ws % kNW;
+                if (!mbar_wait(&w_empty[wsl], ((ws / kNW) & 1) ^ 1, abort_flag, err)) break;
+                mbar_arrive_expect_tx(&w_full[wsl], kWStageBytes);
+                tma_load_2d(wring + wsl * kWStageBytes, &wmap, ws * kWRowBytes, n0, &w_full[wsl]);
+                ++issued_w;
+                bool ok = true;
+                for (int sub = 0; sub < kKW / kKB; ++sub) {
+                    const int s = ws * (kKW / kKB) + sub, xsl = s % kNX;
+                    if (!mbar_wait(&x_empty[xsl], ((s / kNX) & 1) ^ 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&x_full[xsl], Cfg::kXStage);
+                    tma_load_2d(xring + xsl * Cfg::kXStage, &xmap, s * kKB, m0, &x_full[xsl]);
+                    ++issued_x;
+                }
+                if (!ok) break;
+            }
+            // let every issued copy land before the CTA can exit
+            for (int i = issued_w - kNW; i < issued_w; ++i)
+                if (i >= 0) mbar_drain(&w_full[i % kNW], (i / kNW) & 1);
+            for (int i = issued_x - kNX; i < issued_x; ++i)
+                if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(kTileN, TM);
+            for (int s = 0; s < KS; ++s) {
+                const int xsl = s % kNX, asl = s % kNA;
+                if (!mbar_wait(&x_full[xsl], (s / kNX) & 1, abort_flag, err)) break;
+                if (!mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err)) break;
+                tc_fence_after();
+                const uint64_t bdesc = smem_desc_k128(xring + xsl * Cfg::kXStage);
+#pragma unroll
+                for (int kk = 0; kk < kKB / 16; ++kk)
+                    mma_f16_ts(d_tmem, a_tmem + asl * 32 + kk * 8, bdesc + 2 * kk, idesc,
+                               (s | kk) != 0);
+                mma_commit(&x_empty[xsl]);
+                mma_commit(&a_empty[asl]);
+            }
+            mma_commit(d_full);
+        }
+    } else {
+        // warps 2..5: dequantise into TMEM, then the epilogue
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // weight row within the tile
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        bool ok = true;
+        for (int ws = 0; ws < KWS && ok; ++ws) {
+            const int wsl = ws % kNW;
+            ok = __all_sync(0xffffffffu, mbar_wait(&w_full[wsl], (ws / kNW) & 1, abort_flag, err));
+            if (!ok) break;
+            const uint8_t *row = wring + wsl * kWStageBytes + r * kWRowBytes;
+            for (int sub = 0; sub < kKW / kKB; ++sub) {
+                const int s = ws * (kKW / kKB) + sub, asl = s % kNA;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(row + sub * 36);
+                uint32_t wv[9];
+#pragma unroll
+                for (int i = 0; i < 9; ++i) wv[i] = src[i];
+                const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16),
+                                        __funnelshift_r(wv[1], wv[2], 16),
+                                        __funnelshift_r(wv[2], wv[3], 16),
+                                        __funnelshift_r(wv[3], wv[4], 16)};
+                const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+                uint32_t cols[32];
+                dequant_block(wv[0] & 0xFFFFu, Q0, cols);
+                dequant_block(wv[4] >> 16, Q1, cols + 16);
+                tmem_st32(a_tmem + lane_base + asl * 32, cols);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&a_full[asl]);
+            }
+            if (!ok) break;
+            mbar_arrive(&w_empty[wsl]);
+        }
+        // epilogue: D[row r][column m] -> y[m][n0 + r]
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));
+        if (ok) {
+            tc_fence_after();
+            const int n = n0 + r;
+            for (int c = 0; c < (int)Cfg::kDCols; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(d_tmem + lane_base + c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int m = m0 + c + j;
+                    if (c + j < TM && m < M && n < N) y[(int64_t)m * N + n] = __uint_as_float(v[j]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        if (lane == 0) {
+            // every MMA issued by this CTA has finished before TMEM is released
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kCols);
+    }
+}
+
+// ----------------------------------------------------------------- host
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+template <int TM>
+cudaError_t launch_tm(const void *x16, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+                      cudaStream_t s, unsigned int *err) {
+    using Cfg = GemmCfg<TM>;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap xmap, wmap;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {kKB, TM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x16), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t rowbytes = (cuuint64_t)(K / 32) * 18;
+        const cuuint64_t dims[2] = {rowbytes, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {rowbytes};
+        const cuuint32_t box[2] = {kWRowBytes, kTileN};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(wq), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_kernel<TM>), (int)Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM));
+    gemm_kernel<TM><<<grid, kThreads, Cfg::kSmem, s>>>(xmap, wmap, y, (int)M, (int)N, (int)K, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t M, int64_t K) {
+    return (size_t)(((M * K * 2) + 255) / 256 * 256);
+}
+
+cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+                        int64_t K, void *x16, cudaStream_t s, unsigned int *err) {
+    const int64_t n8 = M * K / 8;
+    const int64_t blocks = (n8 + 255) / 256;
+    if (blocks > 0x7FFFFFFF || (M + 15) / 16 > 65535) return cudaErrorInvalidValue;
+    x_to_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x),
+                                                     reinterpret_cast<uint4 *>(x16), n8);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (M > 128) return launch_tm<256>(x16, wq, y, M, N, K, s, err);
+    if (M > 64) return launch_tm<128>(x16, wq, y, M, N, K, s, err);
+    if (M > 32) return launch_tm<64>(x16, wq, y, M, N, K, s, err);
+    if (M > 16) return launch_tm<32>(x16, wq, y, M, N, K, s, err);
+    return launch_tm<16>(x16, wq, y, M, N, K, s, err);
+}
+
+}  // namespace q4_0

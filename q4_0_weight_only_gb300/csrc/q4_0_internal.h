@@ -1,0 +1,31 @@
+// q4_0_internal.h -- launchers shared between the translation units of
+// libq4_0.so (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q4_0 {
+
+// Per-device facts, queried once per device.
+int device_sm_count(int device);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device),
+// so that later launches (possibly inside a stream capture) only launch.
+cudaError_t ensure_smem_attr(const void *func, int bytes);
+// Device error word of the current device (a __device__ variable's address).
+unsigned int *device_error_word();
+
+cudaError_t launch_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, cudaStream_t s,
+                            unsigned int *err);
+
+// Decode GEMV for M <= 32 (x, y point at row 0; row strides K and N).
+cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t s, unsigned int *err);
+
+// tcgen05 GEMM; `x16` is caller scratch of gemm_workspace_bytes(M, K).
+size_t gemm_workspace_bytes(int64_t M, int64_t K);
+cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+                        int64_t K, void *x16, cudaStream_t s, unsigned int *err);
+
+}  // namespace q4_0

@@ -1,0 +1,84 @@
+"""The C ABI on a machine without a GPU: the library builds, loads, exports
+every entry point include/q4_0.h declares, and rejects bad arguments before
+touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4_0.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4_0_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from q4_0_weight_only_gb300 import build, _lib
+    build.build()
+    return _lib.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("q4_0_quantize", "q4_0_matmul", "q4_0_status_string", "q4_0_version",
+                     "q4_0_weight_bytes"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from q4_0_weight_only_gb300 import _lib
+    names = declared_functions()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(_lib.SIGNATURES) == names
+
+
+def test_version_and_status_strings(lib):
+    assert lib.q4_0_version() == 1
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        assert lib.q4_0_status_string(code)
+
+
+def test_weight_bytes(lib):
+    assert lib.q4_0_weight_bytes(256, 1024) == 256 * 32 * 18
+    assert lib.q4_0_weight_bytes(7168, 5120) == 20643840
+    assert lib.q4_0_weight_bytes(1, 33) == 0
+    assert lib.q4_0_weight_bytes(0, 32) == 0
+
+
+def test_workspace_sizes(lib):
+    assert lib.q4_0_matmul_workspace_bytes(1, 5120, 5120) == 0
+    assert lib.q4_0_matmul_workspace_bytes(32, 5120, 5120) == 0
+    assert lib.q4_0_matmul_workspace_bytes(33, 5120, 5120) == 33 * 5120 * 2
+    assert lib.q4_0_gemm_workspace_bytes(3, 256) % 256 == 0
+
+
+def test_invalid_arguments_rejected_before_cuda(lib):
+    P = ctypes.c_void_p
+    good = P(1 << 20)  # never dereferenced: validation fails first
+    assert lib.q4_0_matmul(None, good, good, 1, 1, 256, None) == -1
+    assert lib.q4_0_matmul(good, good, good, 0, 1, 256, None) == -1
+    assert lib.q4_0_matmul(good, good, good, 1, 0, 256, None) == -1
+    assert lib.q4_0_matmul(good, good, good, 1, 1, 48, None) == -1     # K % 32
+    assert lib.q4_0_matmul(good, good, good, 1, 1, 96, None) == -2     # K % 256
+    assert lib.q4_0_matmul(P((1 << 20) + 8), good, good, 1, 1, 256, None) == -1  # misaligned
+    assert lib.q4_0_gemv(good, good, good, 33, 1, 256, None) == -2
+    assert lib.q4_0_gemm(good, good, good, 64, 1, 256, None, 0, None) == -5
+    assert lib.q4_0_gemm(good, good, good, 64, 1, 256, P((1 << 20) + 16), 1 << 20, None) == -5
+    assert lib.q4_0_quantize(None, good, 1, 32, None) == -1
+    assert lib.q4_0_quantize(good, good, 1, 31, None) == -1
+    assert lib.q4_0_device_error(None) == -1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from q4_0_weight_only_gb300 import _lib
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError):
+        _lib.lib()

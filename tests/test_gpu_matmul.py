@@ -1,0 +1,150 @@
+"""Q4_0 matmul on the device against the oracle (all through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import check_full, check_sampled, lib, wq_dev, x_dev
+from q4_0_weight_only_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def case(seed, M, N, K, outlier_blocks=0.0, act_outliers=0.0):
+    w, x = synth.small_case(seed, M, N, K, outlier_block_frac=outlier_blocks,
+                            act_outlier_frac=act_outliers)
+    return x, oracle.get().quantize(w)
+
+
+# ------------------------------------------------------------ small, full
+
+SMALL_GEMV = [(1, 1, 256), (1, 2, 256), (1, 3, 512), (1, 200, 1280), (1, 257, 2304),
+              (2, 129, 1024), (3, 64, 768), (4, 300, 2048), (5, 77, 4352), (8, 1000, 1280),
+              (13, 33, 2560), (16, 512, 1024), (31, 65, 1536), (32, 256, 3072)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_GEMV)
+def test_gemv_small(M, N, K):
+    q4 = lib()
+    x, wq = case(1000 + M * 7 + N, M, N, K, outlier_blocks=0.05, act_outliers=0.01)
+    check_full(q4.gemv(x_dev(x), wq_dev(wq), N, K), x, wq, N, K)
+
+
+SMALL_GEMM = [(1, 128, 256), (16, 128, 256), (17, 200, 512), (32, 384, 768), (33, 128, 256),
+              (64, 1000, 1280), (65, 129, 2304), (100, 256, 1024), (128, 640, 512),
+              (129, 300, 768), (256, 128, 1024), (300, 520, 1536), (513, 384, 512)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_GEMM)
+def test_gemm_small(M, N, K):
+    q4 = lib()
+    x, wq = case(2000 + M * 7 + N, M, N, K, outlier_blocks=0.05)
+    check_full(q4.gemm(x_dev(x), wq_dev(wq), N, K), x, wq, N, K)
+
+
+def test_dispatch_matches_kernels_bitwise():
+    q4 = lib()
+    for M in (1, 7, 32, 33, 200):
+        x, wq = case(3000 + M, M, 384, 1024)
+        xd, wd = x_dev(x), wq_dev(wq)
+        y = q4.matmul(xd, wd, 384, 1024)
+        ref = q4.gemv(xd, wd, 384, 1024) if M <= 32 else q4.gemm(xd, wd, 384, 1024)
+        assert torch.equal(y, ref)
+        assert torch.equal(q4.matmul_alloc(xd, wd, 384, 1024), y)
+
+
+def test_gemv_and_gemm_agree():
+    q4 = lib()
+    for M in (1, 16, 32):
+        x, wq = case(4000 + M, M, 512, 2048, act_outliers=0.01)
+        xd, wd = x_dev(x), wq_dev(wq)
+        a = q4.gemv(xd, wd, 512, 2048).double().cpu().numpy()
+        b = q4.gemm(xd, wd, 512, 2048).double().cpu().numpy()
+        _, absum = oracle.get().matmul(x, wq, 512, 2048)
+        assert oracle.check(a, b, absum)["ok"]
+
+
+def test_deterministic():
+    q4 = lib()
+    for M, N, K in ((1, 5000, 5120), (8, 700, 2048), (300, 500, 1024)):
+        x, wq = case(5000 + M, M, N, K)
+        xd, wd = x_dev(x), wq_dev(wq)
+        y1 = q4.matmul(xd, wd, N, K).clone()
+        y2 = q4.matmul(xd, wd, N, K)
+        assert torch.equal(y1, y2)
+
+
+def test_output_guards_untouched():
+    q4 = lib()
+    for M, N, K in ((1, 33, 256), (5, 130, 512), (70, 130, 512)):
+        x, wq = case(6000 + M, M, N, K)
+        pad = 64
+        buf = torch.full((M * N + 2 * pad,), float("nan"), device="cuda")
+        out = buf[pad:pad + M * N].view(M, N)
+        q4.matmul(x_dev(x), wq_dev(wq), N, K, out=out)
+        assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + M * N:]).all()
+        check_full(out, x, wq, N, K)
+
+
+def test_device_argument_errors():
+    q4 = lib()
+    x, wq = case(7000, 40, 128, 256)
+    xd, wd = x_dev(x), wq_dev(wq)
+    with pytest.raises(q4.Q4Error) as e:
+        q4.gemm(xd, wd, 128, 256, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == q4.ERR_WORKSPACE
+    big = torch.empty(2 * 40 * 256 + 8, dtype=torch.bfloat16, device="cuda")
+    shifted = big[1:1 + 40 * 256].view(40, 256)       # 2-byte aligned only
+    shifted.copy_(xd)
+    with pytest.raises(q4.Q4Error) as e:
+        q4.matmul(shifted, wd, 128, 256)
+    assert e.value.status == q4.ERR_INVALID_ARG
+    assert q4.device_error() == 0
+
+
+# --------------------------------------------------------- workload sizes
+
+def test_pr1():
+    q4 = lib()
+    w, x = synth.pr1()
+    wq = oracle.get().quantize(w)
+    check_full(q4.matmul(x_dev(x), wq_dev(wq), 256, 1024), x, wq, 256, 1024)
+
+
+@pytest.mark.parametrize("shape", synth.SHAPE_ORDER)
+def test_decode_full(shape):
+    q4 = lib()
+    N, K = synth.SHAPES[shape]
+    w, x = synth.decode(shape)
+    wq = oracle.get().quantize(w)
+    check_full(q4.matmul(x_dev(x), wq_dev(wq), N, K), x, wq, N, K)
+
+
+@pytest.mark.parametrize("shape", synth.SHAPE_ORDER)
+def test_batched(shape):
+    q4 = lib()
+    N, K = synth.SHAPES[shape]
+    wq = oracle.get().quantize(synth.decode_weights(shape))
+    wd = wq_dev(wq)
+    for M in synth.BATCHED_M:
+        x = synth.batched_x(shape, M)
+        y = q4.matmul(x_dev(x), wd, N, K)
+        if M == 4 and shape in ("o", "qkv"):
+            check_full(y, x, wq, N, K)
+        else:
+            check_sampled(y, x, wq, N, K, seed=M)
+
+
+@pytest.mark.parametrize("shape", synth.SHAPE_ORDER)
+def test_prefill(shape):
+    q4 = lib()
+    N, K = synth.SHAPES[shape]
+    wq = oracle.get().quantize(synth.prefill_weights(shape))
+    wd = wq_dev(wq)
+    for M in synth.PREFILL_M:
+        x = synth.prefill_x(shape, M)
+        y = q4.matmul(x_dev(x), wd, N, K)
+        check_sampled(y, x, wq, N, K, seed=M)
+        del y
+        torch.cuda.empty_cache()
+    assert q4.device_error() == 0
