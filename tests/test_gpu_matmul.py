@@ -90,9 +90,14 @@ def test_device_argument_errors():
     q4 = lib()
     x, wq = case(7000, 40, 128, 256)
     xd, wd = x_dev(x), wq_dev(wq)
-    with pytest.raises(q4.Q4Error) as e:
-        q4.gemm(xd, wd, 128, 256, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
-    assert e.value.status == q4.ERR_WORKSPACE
+    y = torch.empty((40, 128), dtype=torch.float32, device="cuda")
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    st = q4.lib().q4_0_gemm(xd.data_ptr(), wd.data_ptr(), y.data_ptr(), 40, 128, 256,
+                            small.data_ptr(), small.numel(), None)
+    assert st == q4.ERR_WORKSPACE
+    st = q4.lib().q4_0_matmul_ws(xd.data_ptr(), wd.data_ptr(), y.data_ptr(), 40, 128, 256,
+                                 None, 0, None)
+    assert st == q4.ERR_WORKSPACE
     big = torch.empty(2 * 40 * 256 + 8, dtype=torch.bfloat16, device="cuda")
     shifted = big[1:1 + 40 * 256].view(40, 256)       # 2-byte aligned only
     shifted.copy_(xd)
