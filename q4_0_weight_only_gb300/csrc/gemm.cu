@@ -62,6 +62,8 @@ __device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint
 // bf16 -> binary16 (round to nearest even), 8 elements per thread.
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__ x,
                                                        uint4 *__restrict__ x16, int64_t n8) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n8) return;
     const uint4 u = __ldg(x + i);
@@ -140,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_launch_dependents();
+    pdl_wait();  // x16 comes from the previous kernel
     const uint32_t tmem = *tmem_slot;
     const uint32_t d_tmem = tmem;
     const uint32_t a_tmem = tmem + Cfg::kDCols;
@@ -310,8 +314,8 @@ cudaError_t launch_tm(const void *x16, const uint8_t *wq, float *y, int64_t M, i
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_kernel<TM>), (int)Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM));
-    gemm_kernel<TM><<<grid, kThreads, Cfg::kSmem, s>>>(xmap, wmap, y, (int)M, (int)N, (int)K, err);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel<TM>, grid, dim3(kThreads), Cfg::kSmem, s, xmap, wmap, y, (int)M,
+                      (int)N, (int)K, err);
 }
 
 }  // namespace
@@ -325,9 +329,8 @@ cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t 
     const int64_t n8 = M * K / 8;
     const int64_t blocks = (n8 + 255) / 256;
     if (blocks > 0x7FFFFFFF || (M + 15) / 16 > 65535) return cudaErrorInvalidValue;
-    x_to_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x),
-                                                     reinterpret_cast<uint4 *>(x16), n8);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(x_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+                               reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(x16), n8);
     if (e != cudaSuccess) return e;
     if (M > 128) return launch_tm<256>(x16, wq, y, M, N, K, s, err);
     if (M > 64) return launch_tm<128>(x16, wq, y, M, N, K, s, err);

@@ -137,9 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_g2s(dst, src, bytes, bar);
         if (hasB) bulk_g2s(dst + kRowChunkBytes, src + rowbytes, bytes, bar);
     };
+    pdl_launch_dependents();
     if (lane == 0) {
         for (int j = 0; j < kSlots && j < my_items; ++j) issue(j);
     }
+    pdl_wait();
 
     // x -> shared memory, per (row m, block b): e = exponent of max|x| so
     // that |x * 2^-e| < 1; quads of half2 in the order block_dot reads them;
@@ -281,11 +283,342 @@ cudaError_t launch_mt(const uint16_t *x, const uint8_t *wq, float *y, const Gemv
                       int grid, cudaStream_t s, unsigned int *err) {
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_kernel<MT>), (int)p.smem);
     if (e != cudaSuccess) return e;
-    gemv_kernel<MT><<<grid, kThreads, p.smem, s>>>(x, wq, y, p.args, err);
-    return cudaGetLastError();
+    return launch_pdl(gemv_kernel<MT>, dim3(grid), dim3(kThreads), p.smem, s, x, wq, y, p.args, err);
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
+
+// ---------------------------------------------------------------------------
+// Integer-dot decode kernel (M <= 2, K % 1024 == 0).
+//
+// x is turned, per 32-element block, into 15-bit fixed point X = round(x *
+// 2^(14-e)) with 2^e > max|x| of the block, split into a signed high byte and
+// an unsigned low byte (X = 256 Xh + Xl).  A Q4_0 block then needs
+//   sum_j (q_j - 8) x_j = 2^(e-14) * (256 * sum q Xh + sum q Xl - 8 sum X),
+// two exact 4-way byte dot products (dp4a) per four weights, the -8 sum X
+// term precomputed once per block of x.  Scale apply: one fp32 FMA per block
+// with d * 2^(e-14).  The integer sums are exact (|.| < 2^24), so the only
+// rounding beyond fp32 accumulation is X's fixed point for elements far below
+// their block's maximum.
+//
+// Thread (rs, pc) owns block pair pc (64 weights) of every c-th row: its x
+// bytes stay in registers for the whole kernel.  A producer warp streams
+// stages of R whole rows (contiguous bytes) with one bulk TMA copy each; a
+// row's 2P pair partials are reduced by 16-lane butterflies into P/16
+// half-warp partials, summed in order at the end.
+// ---------------------------------------------------------------------------
+namespace dp {
+
+template <int MT>
+struct Limits {
+    static constexpr int kThreads = MT == 1 ? 896 : 640;  // keeps x bytes in registers without spills
+};
+
+struct Args {
+    int64_t N, K;
+    int P, c, T, R, S, rowbytes, H, mrows;
+    uint32_t stage_bytes, off_x, off_bars, off_part;
+};
+
+// Fixed-point x of one block pair, as kept in shared memory and registers:
+// words 0-15 Xh bytes (block 0 words 0-7, block 1 words 8-15), 16-31 Xl
+// bytes, 32-33 -8 * sum X per block, 34-35 2^(e-14) per block.
+constexpr int kPairWords = 36;
+
+template <int MT>
+struct XReg {
+    uint32_t h[MT][16];
+    uint32_t l[MT][16];
+    int ncorr[MT][2];
+    float xs[MT][2];
+};
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Block b of x row m (32 bf16 values) -> fixed point, written into the
+// pair record of shared memory.
+__device__ __forceinline__ void convert_block(const uint16_t *__restrict__ xrow, int b,
+                                              uint32_t *__restrict__ rec) {
+    float xv[32];
+    if (xrow) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(xrow + (int64_t)b * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 u = __ldg(src + i);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                xv[8 * i + 2 * h] = __uint_as_float(w4[h] << 16);
+                xv[8 * i + 2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xv[j] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(xv[j]));
+    int e = 0;
+    if (amax > 0.f) {
+        frexpf(amax, &e);
+        e = max(-100, min(127, e));
+    }
+    const float up = amax > 0.f ? ldexpf(1.0f, 14 - e) : 0.f;
+    const int blk = b & 1;
+    int sum = 0;
+#pragma unroll
+    for (int wd = 0; wd < 8; ++wd) {
+        int X[4];
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+            X[bb] = __float2int_rn(xv[4 * wd + bb] * up);
+            sum += X[bb];
+        }
+        // bytes 1 (high) and 0 (low) of the four 16-bit fixed-point values
+        rec[blk * 8 + wd] = __byte_perm(__byte_perm(X[0], X[1], 0x0051), __byte_perm(X[2], X[3], 0x0051), 0x5410);
+        rec[16 + blk * 8 + wd] = __byte_perm(__byte_perm(X[0], X[1], 0x0040), __byte_perm(X[2], X[3], 0x0040), 0x5410);
+    }
+    reinterpret_cast<int *>(rec)[32 + blk] = -8 * sum;
+    reinterpret_cast<float *>(rec)[34 + blk] = amax > 0.f ? ldexpf(1.0f, e - 14) : 0.f;
+}
+
+// One Q4_0 block against MT rows of x: v[m] += d * 2^(e-14) * T.
+template <int MT>
+__device__ __forceinline__ void block_dp(uint32_t dbits, const uint32_t (&Q)[4], const XReg<MT> &r,
+                                         int blk, float (&v)[MT]) {
+    uint32_t lo[4], hi[4];
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        lo[wi] = Q[wi] & 0x0F0F0F0Fu;         // elements 4wi .. 4wi+3
+        hi[wi] = (Q[wi] >> 4) & 0x0F0F0F0Fu;  // elements 16+4wi .. 16+4wi+3
+    }
+    const float d = __half2float(__ushort_as_half((unsigned short)dbits));
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        int ah = 0, al = r.ncorr[m][blk];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+            ah = dp4a_us(lo[wi], r.h[m][blk * 8 + wi], ah);
+            al = dp4a_uu(lo[wi], r.l[m][blk * 8 + wi], al);
+            ah = dp4a_us(hi[wi], r.h[m][blk * 8 + 4 + wi], ah);
+            al = dp4a_uu(hi[wi], r.l[m][blk * 8 + 4 + wi], al);
+        }
+        const int T = ah * 256 + al;
+        v[m] = fmaf((float)T, d * r.xs[m][blk], v[m]);
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(Limits<MT>::kThreads, 1)
+    gemv_dp4a_kernel(const uint16_t *__restrict__ x, const uint8_t *__restrict__ wq,
+                     float *__restrict__ y, const Args a, unsigned int *err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t *xsm = reinterpret_cast<uint32_t *>(smem + a.off_x);  // [MT][P][36]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bars);
+    uint64_t *empty = full + a.S;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + a.S);
+    float *part = reinterpret_cast<float *>(smem + a.off_part);  // [rows][H][MT]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nwc = a.T >> 5;
+    const int64_t r0 = (int64_t)blockIdx.x * a.N / gridDim.x;
+    const int64_t r1 = (int64_t)(blockIdx.x + 1) * a.N / gridDim.x;
+    const int nrows = (int)(r1 - r0);
+    const int nst = (nrows + a.R - 1) / a.R;
+
+    if (tid == 0) {
+        for (int i = 0; i < a.S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], nwc);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == nwc) {
+        // producer: stage i = rows [r0 + i R, r0 + i R + R), one bulk copy.
+        // Weights are read before pdl_wait(): no kernel of this library
+        // writes Q4_0 weights while a dependent matmul may be running.
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int s = i % a.S;
+                if (!mbar_wait(&empty[s], ((i / a.S) & 1) ^ 1, abort_flag, err)) break;
+                const int rows = min(a.R, nrows - i * a.R);
+                const uint32_t bytes = (uint32_t)rows * (uint32_t)a.rowbytes;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                bulk_g2s(smem + (size_t)s * a.stage_bytes, wq + (r0 + (int64_t)i * a.R) * a.rowbytes,
+                         bytes, &full[s]);
+                ++issued;
+            }
+            for (int i = max(0, issued - a.S); i < issued; ++i)
+                mbar_drain(&full[i % a.S], (i / a.S) & 1);
+        }
+        return;
+    }
+
+    // x -> fixed point in shared memory, once per CTA (overlaps the first copies)
+    pdl_wait();
+    const int nb = 2 * a.P;
+    for (int t = tid; t < MT * nb; t += a.T) {
+        const int m = t / nb, b = t - m * nb;
+        convert_block(m < a.mrows ? x + (int64_t)m * a.K : nullptr, b,
+                      xsm + ((size_t)m * a.P + (b >> 1)) * kPairWords);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(a.T) : "memory");
+
+    const int pc = tid % a.P, rs = tid / a.P;
+    const bool active = rs < a.c;
+    XReg<MT> xr;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const uint4 *rec = reinterpret_cast<const uint4 *>(xsm + ((size_t)m * a.P + pc) * kPairWords);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 u = rec[i], w = rec[4 + i];
+            xr.h[m][4 * i] = u.x; xr.h[m][4 * i + 1] = u.y; xr.h[m][4 * i + 2] = u.z; xr.h[m][4 * i + 3] = u.w;
+            xr.l[m][4 * i] = w.x; xr.l[m][4 * i + 1] = w.y; xr.l[m][4 * i + 2] = w.z; xr.l[m][4 * i + 3] = w.w;
+        }
+        const uint4 t = rec[8];
+        xr.ncorr[m][0] = (int)t.x;
+        xr.ncorr[m][1] = (int)t.y;
+        xr.xs[m][0] = __uint_as_float(t.z);
+        xr.xs[m][1] = __uint_as_float(t.w);
+    }
+
+    const int per_thread = a.R / a.c;  // same trip count on every lane
+    for (int i = 0; i < nst; ++i) {
+        const int s = i % a.S;
+        const bool ok = mbar_wait(&full[s], (i / a.S) & 1, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int rows = min(a.R, nrows - i * a.R);
+        const uint8_t *st = smem + (size_t)s * a.stage_bytes;
+        for (int it = 0; it < per_thread; ++it) {
+            const int rr = rs + it * a.c;
+            const bool valid = active && rr < rows;
+            float v[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) v[m] = 0.f;
+            if (valid) {
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(st + (size_t)rr * a.rowbytes + pc * 36);
+                uint32_t wv[9];
+#pragma unroll
+                for (int k = 0; k < 9; ++k) wv[k] = src[k];
+                const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
+                                        __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
+                const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+                block_dp<MT>(wv[0] & 0xFFFFu, Q0, xr, 0, v);
+                block_dp<MT>(wv[4] >> 16, Q1, xr, 1, v);
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float t = v[m];
+                t += __shfl_xor_sync(0xffffffffu, t, 8);
+                t += __shfl_xor_sync(0xffffffffu, t, 4);
+                t += __shfl_xor_sync(0xffffffffu, t, 2);
+                t += __shfl_xor_sync(0xffffffffu, t, 1);
+                v[m] = t;
+            }
+            if (valid && (lane & 15) == 0) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    part[((size_t)(i * a.R + rr) * a.H + (pc >> 4)) * MT + m] = v[m];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(a.T) : "memory");
+    for (int t = tid; t < nrows * a.mrows; t += a.T) {
+        const int m = t / nrows, r = t - m * nrows;
+        float sum = 0.f;
+        for (int h = 0; h < a.H; ++h) sum += part[((size_t)r * a.H + h) * MT + m];
+        y[(int64_t)m * a.N + r0 + r] = sum;
+    }
+}
+
+struct Plan {
+    Args a;
+    size_t smem;
+    int threads;
+    bool ok;
+};
+
+// One CTA per SM: c row slots of P threads (P = K / 64 block pairs), a
+// producer warp, and as many row stages of about 20 KB as shared memory holds.
+Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
+    Plan p{};
+    Args &a = p.a;
+    a.N = N;
+    a.K = K;
+    a.P = (int)(K / 64);
+    p.ok = (K % 1024 == 0);
+    if (!p.ok) return p;
+    const int max_threads = mt == 1 ? Limits<1>::kThreads : Limits<2>::kThreads;
+    const int budget = max_threads - 32;
+    a.c = max(1, budget / a.P);
+    if ((a.c * a.P) % 32 != 0 && a.c > 1) a.c &= ~1;  // keep row slots on half-warp boundaries
+    a.T = ((a.c * a.P + 31) / 32) * 32;
+    p.threads = a.T + 32;
+    if (p.threads > max_threads || a.P % 16 != 0) {
+        p.ok = false;
+        return p;
+    }
+    a.rowbytes = (int)(K / 32 * 18);
+    const int per = a.c * a.rowbytes;
+    a.R = a.c * max(1, (20480 + per / 2) / per);
+    a.H = a.P / 16;
+    a.stage_bytes = (uint32_t)a.R * (uint32_t)a.rowbytes;
+    const int64_t rows_cap = (N + grid - 1) / grid + 1;
+    const size_t fixed = (size_t)mt * a.P * kPairWords * 4 + (size_t)rows_cap * a.H * mt * 4 + 16 * 8 + 64;
+    int S = 8;
+    while (S > 2 && (size_t)S * a.stage_bytes + fixed > kSmemLimit) --S;
+    a.S = S;
+    size_t off = (size_t)a.S * a.stage_bytes;
+    off = (off + 127) & ~(size_t)127;
+    a.off_x = (uint32_t)off;
+    off += (size_t)mt * a.P * kPairWords * 4;
+    a.off_bars = (uint32_t)off;
+    off += (size_t)2 * a.S * 8 + 16;
+    a.off_part = (uint32_t)off;
+    off += (size_t)rows_cap * a.H * mt * 4;
+    p.smem = off;
+    p.ok = p.smem <= kSmemLimit;
+    return p;
+}
+
+template <int MT>
+cudaError_t launch(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+                   int sms, cudaStream_t s, unsigned int *err, bool *done) {
+    *done = false;
+    const int grid = (int)(N < sms ? N : sms);
+    Plan p = make_plan(MT, N, K, grid);
+    if (!p.ok) return cudaSuccess;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_dp4a_kernel<MT>), (int)p.smem);
+    if (e != cudaSuccess) return e;
+    for (int64_t m0 = 0; m0 < M; m0 += MT) {
+        p.a.mrows = (int)(M - m0 < MT ? M - m0 : MT);
+        e = launch_pdl(gemv_dp4a_kernel<MT>, dim3(grid), dim3(p.threads), p.smem, s, x + m0 * K, wq,
+                       y + m0 * N, p.a, err);
+        if (e != cudaSuccess) return e;
+    }
+    *done = true;
+    return cudaSuccess;
+}
+
+}  // namespace dp
 
 }  // namespace
 
@@ -298,6 +631,12 @@ cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t 
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int64_t grid64 = (N + 1) / 2 < sms ? (N + 1) / 2 : sms;
     const int grid = (int)grid64;
+    if (M <= 2) {
+        bool done = false;
+        e = M == 1 ? dp::launch<1>(x, wq, y, M, N, K, sms, s, err, &done)
+                   : dp::launch<2>(x, wq, y, M, N, K, sms, s, err, &done);
+        if (e != cudaSuccess || done) return e;
+    }
     // rows of x per launch: the largest power of two <= 8 that covers M (or
     // fits shared memory); each launch streams the weights once
     int mt = 1;

@@ -13,6 +13,25 @@ int device_sm_count(int device);
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device),
 // so that later launches (possibly inside a stream capture) only launch.
 cudaError_t ensure_smem_attr(const void *func, int bytes);
+// Launch with programmatic stream serialization allowed, so the kernel may
+// begin while the previous kernel in the stream is still running (it must
+// call griddepcontrol.wait before reading anything that kernel wrote).
+template <typename... Params, typename... Actual>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Actual &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Actual &&>(args)...);
+}
+
 // Device error word of the current device (a __device__ variable's address).
 unsigned int *device_error_word();
 

@@ -61,6 +61,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` for the phase
+// instead of returning at once (fewer issue slots spent polling).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // kWaitLimitNs (or at once when *abort is set by another thread of the
 // CTA): records the timeout in *err, sets *abort and returns false.
@@ -69,8 +83,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if ((it & 7u) == 0) {
             if (*abort) return false;
             if (global_ns() - t0 > kWaitLimitNs) {
                 atomicExch(err, kErrWaitTimeout);
@@ -90,6 +104,18 @@ __device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity) {
     }
     return true;
 }
+
+// ----------------------------------------------------- dependent launches
+
+// Programmatic dependent launch: the next kernel in the stream may start
+// (its prologue and weight prefetch overlap this kernel's tail) ...
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and blocks here until every kernel it depends on has completed and its
+// writes are visible.  Nothing written by an earlier kernel may be read
+// before this point.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------ TMA
 

@@ -20,7 +20,10 @@ def case(seed, M, N, K, outlier_blocks=0.0, act_outliers=0.0):
 
 SMALL_GEMV = [(1, 1, 256), (1, 2, 256), (1, 3, 512), (1, 200, 1280), (1, 257, 2304),
               (2, 129, 1024), (3, 64, 768), (4, 300, 2048), (5, 77, 4352), (8, 1000, 1280),
-              (13, 33, 2560), (16, 512, 1024), (31, 65, 1536), (32, 256, 3072)]
+              (13, 33, 2560), (16, 512, 1024), (31, 65, 1536), (32, 256, 3072),
+              # K % 1024 == 0 with M <= 2: the integer-dot decode kernel
+              (1, 1, 1024), (1, 3, 2048), (1, 31, 3072), (2, 200, 1024), (2, 257, 4096),
+              (1, 1000, 7168), (2, 5, 17408), (1, 4099, 5120)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALL_GEMV)
