@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *my_ring = ring + warp * kSlots * kSlotBytes;
     uint64_t *my_bars = bars + warp * kSlots;
 
+    const uint64_t policy = l2_evict_first_policy();  // weights are read once
     auto issue = [&](int j) {
         const int it = warp + kWarps * j;
         const int pr = it / C, c = it - pr * C;
@@ -134,8 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t *bar = my_bars + (j % kSlots);
         const uint8_t *src = wq + rowA * rowbytes + (int64_t)c * kRowChunkBytes;
         mbar_arrive_expect_tx(bar, hasB ? 2 * bytes : bytes);
-        bulk_g2s(dst, src, bytes, bar);
-        if (hasB) bulk_g2s(dst + kRowChunkBytes, src + rowbytes, bytes, bar);
+        bulk_g2s_hint(dst, src, bytes, bar, policy);
+        if (hasB) bulk_g2s_hint(dst + kRowChunkBytes, src + rowbytes, bytes, bar, policy);
     };
     pdl_launch_dependents();
     if (lane == 0) {
@@ -309,9 +310,13 @@ constexpr size_t kSmemLimit = 227 * 1024;
 // ---------------------------------------------------------------------------
 namespace dp {
 
+// One CTA per SM holding x in registers: as many threads as the register
+// file allows without spills.
 template <int MT>
 struct Limits {
-    static constexpr int kThreads = MT == 1 ? 896 : 640;  // keeps x bytes in registers without spills
+    static constexpr int kThreads = MT == 1 ? 896 : 640;
+    static constexpr int kCtasPerSm = 1;
+    static constexpr size_t kSmem = 227 * 1024;
 };
 
 struct Args {
@@ -419,7 +424,7 @@ __device__ __forceinline__ void block_dp(uint32_t dbits, const uint32_t (&Q)[4],
 }
 
 template <int MT>
-__global__ void __launch_bounds__(Limits<MT>::kThreads, 1)
+__global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
     gemv_dp4a_kernel(const uint16_t *__restrict__ x, const uint8_t *__restrict__ wq,
                      float *__restrict__ y, const Args a, unsigned int *err) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -431,12 +436,27 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nwc = a.T >> 5;
+    // CTA b owns the contiguous rows [r0, r1); stage i = rows r0 + i R ...
     const int64_t r0 = (int64_t)blockIdx.x * a.N / gridDim.x;
     const int64_t r1 = (int64_t)(blockIdx.x + 1) * a.N / gridDim.x;
-    const int nrows = (int)(r1 - r0);
-    const int nst = (nrows + a.R - 1) / a.R;
+    const int nst = (int)((r1 - r0 + a.R - 1) / a.R);
+    auto stage_row0 = [&](int i) -> int64_t { return r0 + (int64_t)i * a.R; };
+    auto stage_rows = [&](int i) -> int {
+        const int64_t r = stage_row0(i);
+        return (int)(r1 - r < a.R ? r1 - r : a.R);
+    };
+    // weights are streamed once: mark them first to leave L2 so that x and
+    // y (small, reused by the next kernels) stay resident
+    const uint64_t policy = l2_evict_first_policy();
+    auto issue = [&](int i) {
+        const int s = i % a.S;
+        const uint32_t bytes = (uint32_t)stage_rows(i) * (uint32_t)a.rowbytes;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_g2s_hint(smem + (size_t)s * a.stage_bytes, wq + stage_row0(i) * a.rowbytes, bytes, &full[s],
+                      policy);
+    };
 
-    if (tid == 0) {
+    if (warp == nwc && lane == 0) {
         for (int i = 0; i < a.S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], nwc);
@@ -445,22 +465,19 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, 1)
         mbar_fence_init();
     }
     __syncthreads();
+    // trigger the next kernel before anything slow: issuing a bulk copy of a
+    // stage takes a fraction of a microsecond
     pdl_launch_dependents();
 
     if (warp == nwc) {
-        // producer: stage i = rows [r0 + i R, r0 + i R + R), one bulk copy.
         // Weights are read before pdl_wait(): no kernel of this library
         // writes Q4_0 weights while a dependent matmul may be running.
         if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % a.S;
-                if (!mbar_wait(&empty[s], ((i / a.S) & 1) ^ 1, abort_flag, err)) break;
-                const int rows = min(a.R, nrows - i * a.R);
-                const uint32_t bytes = (uint32_t)rows * (uint32_t)a.rowbytes;
-                mbar_arrive_expect_tx(&full[s], bytes);
-                bulk_g2s(smem + (size_t)s * a.stage_bytes, wq + (r0 + (int64_t)i * a.R) * a.rowbytes,
-                         bytes, &full[s]);
+            for (int i = 0; i < a.S && i < nst; ++i) issue(i);
+            int issued = min(a.S, nst);
+            for (int i = a.S; i < nst; ++i) {
+                if (!mbar_wait(&empty[i % a.S], ((i / a.S) & 1) ^ 1, abort_flag, err)) break;
+                issue(i);
                 ++issued;
             }
             for (int i = max(0, issued - a.S); i < issued; ++i)
@@ -498,54 +515,58 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, 1)
         xr.xs[m][1] = __uint_as_float(t.w);
     }
 
-    const int per_thread = a.R / a.c;  // same trip count on every lane
+    // one row per thread per stage: copy the row's block pair to registers,
+    // release the stage to the producer at once, then compute
     for (int i = 0; i < nst; ++i) {
         const int s = i % a.S;
         const bool ok = mbar_wait(&full[s], (i / a.S) & 1, abort_flag, err);
         if (!__all_sync(0xffffffffu, ok)) break;
-        const int rows = min(a.R, nrows - i * a.R);
-        const uint8_t *st = smem + (size_t)s * a.stage_bytes;
-        for (int it = 0; it < per_thread; ++it) {
-            const int rr = rs + it * a.c;
-            const bool valid = active && rr < rows;
-            float v[MT];
+        const int rows = stage_rows(i);
+        const bool valid = active && rs < rows;
+        uint32_t wv[9];
+        if (valid) {
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(smem + (size_t)s * a.stage_bytes +
+                                                                    (size_t)rs * a.rowbytes + pc * 36);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) v[m] = 0.f;
-            if (valid) {
-                const uint32_t *src = reinterpret_cast<const uint32_t *>(st + (size_t)rr * a.rowbytes + pc * 36);
-                uint32_t wv[9];
-#pragma unroll
-                for (int k = 0; k < 9; ++k) wv[k] = src[k];
-                const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
-                                        __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
-                const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
-                block_dp<MT>(wv[0] & 0xFFFFu, Q0, xr, 0, v);
-                block_dp<MT>(wv[4] >> 16, Q1, xr, 1, v);
-            }
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                float t = v[m];
-                t += __shfl_xor_sync(0xffffffffu, t, 8);
-                t += __shfl_xor_sync(0xffffffffu, t, 4);
-                t += __shfl_xor_sync(0xffffffffu, t, 2);
-                t += __shfl_xor_sync(0xffffffffu, t, 1);
-                v[m] = t;
-            }
-            if (valid && (lane & 15) == 0) {
-#pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    part[((size_t)(i * a.R + rr) * a.H + (pc >> 4)) * MT + m] = v[m];
-            }
+            for (int k = 0; k < 9; ++k) wv[k] = src[k];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        float v[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) v[m] = 0.f;
+        if (valid) {
+            const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
+                                    __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
+            const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+            block_dp<MT>(wv[0] & 0xFFFFu, Q0, xr, 0, v);
+            block_dp<MT>(wv[4] >> 16, Q1, xr, 1, v);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float t = v[m];
+            t += __shfl_xor_sync(0xffffffffu, t, 8);
+            t += __shfl_xor_sync(0xffffffffu, t, 4);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            v[m] = t;
+        }
+        if (valid && (lane & 15) == 0) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) part[((size_t)(i * a.R + rs) * a.H + (pc >> 4)) * MT + m] = v[m];
+        }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(a.T) : "memory");
-    for (int t = tid; t < nrows * a.mrows; t += a.T) {
-        const int m = t / nrows, r = t - m * nrows;
+    // fixed-order sum over half-warp partials; consecutive threads write
+    // consecutive rows of a stage
+    const int local_rows = nst * a.R;
+    for (int t = tid; t < local_rows * a.mrows; t += a.T) {
+        const int m = t / local_rows, lr = t - m * local_rows;
+        const int i = lr / a.R, rr = lr - i * a.R;
+        if (rr >= stage_rows(i)) continue;
         float sum = 0.f;
-        for (int h = 0; h < a.H; ++h) sum += part[((size_t)r * a.H + h) * MT + m];
-        y[(int64_t)m * a.N + r0 + r] = sum;
+        for (int h = 0; h < a.H; ++h) sum += part[((size_t)lr * a.H + h) * MT + m];
+        y[(int64_t)m * a.N + stage_row0(i) + rr] = sum;
     }
 }
 
@@ -567,9 +588,9 @@ Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
     p.ok = (K % 1024 == 0);
     if (!p.ok) return p;
     const int max_threads = mt == 1 ? Limits<1>::kThreads : Limits<2>::kThreads;
+    const size_t smem_limit = mt == 1 ? Limits<1>::kSmem : Limits<2>::kSmem;
     const int budget = max_threads - 32;
-    a.c = max(1, budget / a.P);
-    if ((a.c * a.P) % 32 != 0 && a.c > 1) a.c &= ~1;  // keep row slots on half-warp boundaries
+    a.c = max(1, budget / a.P);  // P % 16 == 0: row slots start on half-warp boundaries
     a.T = ((a.c * a.P + 31) / 32) * 32;
     p.threads = a.T + 32;
     if (p.threads > max_threads || a.P % 16 != 0) {
@@ -577,14 +598,13 @@ Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
         return p;
     }
     a.rowbytes = (int)(K / 32 * 18);
-    const int per = a.c * a.rowbytes;
-    a.R = a.c * max(1, (20480 + per / 2) / per);
+    a.R = a.c;  // a stage is one row per row slot
     a.H = a.P / 16;
     a.stage_bytes = (uint32_t)a.R * (uint32_t)a.rowbytes;
-    const int64_t rows_cap = (N + grid - 1) / grid + 1;
+    const int64_t rows_cap = ((N + grid - 1) / grid + a.R) / a.R * a.R;
     const size_t fixed = (size_t)mt * a.P * kPairWords * 4 + (size_t)rows_cap * a.H * mt * 4 + 16 * 8 + 64;
     int S = 8;
-    while (S > 2 && (size_t)S * a.stage_bytes + fixed > kSmemLimit) --S;
+    while (S > 2 && (size_t)S * a.stage_bytes + fixed > smem_limit) --S;
     a.S = S;
     size_t off = (size_t)a.S * a.stage_bytes;
     off = (off + 127) & ~(size_t)127;
@@ -595,7 +615,7 @@ Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
     a.off_part = (uint32_t)off;
     off += (size_t)rows_cap * a.H * mt * 4;
     p.smem = off;
-    p.ok = p.smem <= kSmemLimit;
+    p.ok = p.smem <= smem_limit;
     return p;
 }
 
