@@ -146,6 +146,29 @@ int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y,
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * q4_0_gemm_noalloc -- q4_0_gemm for callers that cannot allocate device
+ * memory and have no workspace to hand over.  The paper has no counterpart:
+ * this entry point exists for callers where the CUDA allocator must not be
+ * entered (host callbacks, real-time loops with no allocation after
+ * start-up, plug-ins whose host owns every device byte).
+ *   x, wq, y, M, N, K, stream : as in q4_0_gemm (same kernels, same result).
+ * Scratch: a fixed array of Q4_0_NOALLOC_SCRATCH_BYTES in device memory,
+ * reserved when the library is loaded on a GPU and held until the process
+ * exits; nothing is allocated or freed per call.  It fits M * K * 2 bytes,
+ * i.e. M * K <= 16 Mi elements; larger calls return Q4_0_ERR_WORKSPACE and
+ * launch nothing.
+ * The array is shared by every call on a device: calls whose kernels overlap
+ * on the GPU (unordered streams) race on it -- order them on one stream.
+ * The first call on each device looks up the array's address; make it before
+ * any stream capture begins.
+ * Returns Q4_0_OK, Q4_0_ERR_INVALID_ARG, Q4_0_ERR_UNSUPPORTED,
+ * Q4_0_ERR_WORKSPACE or Q4_0_ERR_CUDA.
+ */
+#define Q4_0_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int q4_0_gemm_noalloc(const uint16_t *x, const uint8_t *wq, float *y,
+                      int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * q4_0_device_error -- read and clear the device error word of the current
  * device.  Synchronises the device.  *code receives Q4_0_OK or
  * Q4_0_ERR_DEVICE_TIMEOUT (a kernel gave up on a bounded wait and left its

@@ -35,6 +35,7 @@ SIGNATURES = {
     "q4_0_gemv": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "q4_0_gemm_workspace_bytes": ([_I64, _I64], _SZ),
     "q4_0_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
+    "q4_0_gemm_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "q4_0_device_error": ([ctypes.POINTER(_INT)], _INT),
 }
 
@@ -178,6 +179,18 @@ def gemm(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = 
     ws, wsb = _workspace(int(lib().q4_0_gemm_workspace_bytes(M, K)), x.device, workspace)
     _check(lib().q4_0_gemm(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
                            ws.data_ptr(), wsb, _stream(stream)), "q4_0_gemm")
+    return out
+
+
+def gemm_noalloc(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
+                 stream=None) -> torch.Tensor:
+    """The tcgen05 kernel with the library's fixed scratch array instead of a
+    workspace: nothing is allocated on the device by the call (out may be
+    given too).  Calls that overlap on the GPU share the array; see
+    q4_0_gemm_noalloc in include/q4_0.h."""
+    M, out = _mm_args(x, wq, N, K, out)
+    _check(lib().q4_0_gemm_noalloc(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
+                                   _stream(stream)), "q4_0_gemm_noalloc")
     return out
 
 
