@@ -294,7 +294,8 @@ def run_ours(args, rank, world, local):
     if M < 256:
         roof = {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(gbs / world / hbm, 4), "traffic": None,
-                "kernel": "gemv_kernel<1>" if M == 1 else "gemv_kernel", "peak_source": peak_kind,
+                "kernel": "gemv_dp4a_kernel<1>" if M == 1 else ("gemv_dp4a_kernel<2>" if M == 2 else "gemv_kernel"),
+                "peak_source": peak_kind, "bytes_per_launch": round(step_bytes / launches_per_step),
                 "avg_launch_us": round(ms_local * 1e3 / launches, 3)}
     else:
         roof = {"bound": "tensor", "achieved": round(tflops / world, 1), "peak": tf_sust,
@@ -338,15 +339,22 @@ def workload_name(w, M, layers):
 
 
 def load_traffic(workload):
-    """dram bytes per launch from the committed ncu summary, if it covers the
-    current kernels (written by hand from an ncu capture; see profiles/)."""
+    """DRAM bytes per launch of the dominant kernel, from the committed ncu
+    summary (profiles/traffic.json); None when there is none for this
+    workload or the kernel source has changed since it was captured."""
+    import hashlib
     path = os.path.join(HERE, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         with open(path) as f:
-            d = json.load(f)
-        return d.get(workload)
+            d = json.load(f).get(workload)
+        if not d:
+            return None
+        with open(os.path.join(HERE, d["kernel_source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != d["sha256_16"]:
+                return None
+        return d["bytes_per_launch"]
     except Exception:
         return None
 
