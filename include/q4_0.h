@@ -92,13 +92,14 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
  *   M, N, K: M >= 1, N >= 1, K >= 256, K % 256 == 0 (K % 32 != 0 is
  *         INVALID_ARG; K % 32 == 0 but K % 256 != 0 is UNSUPPORTED).
  * y[m][n] = sum_k d(n,k) * (q(n,k) - 8) * x[m][k], accumulated in fp32.
- * Dispatch: M <= 32 runs the decode GEMV (weights streamed once, fp32
- * accumulation of per-block fp16 partial sums); M > 32 runs the tcgen05 GEMM
- * (weights dequantised to binary16 tiles, x rounded to binary16, fp32
- * accumulation in tensor memory).  Both meet: per element
+ * Dispatch: M <= 2 runs the decode GEMV on CUDA cores (exact integer dot
+ * products per 32-weight block on 15-bit fixed-point x, fp32 across blocks);
+ * 3 <= M <= 32 runs the batched decode on the tensor cores; M > 32 runs the
+ * tcgen05 GEMM (weights dequantised to binary16 tiles, x rounded to
+ * binary16, fp32 accumulation in tensor memory).  All meet: per element
  * |y - y_exact| <= 1e-2 * sum_k |w x| and relative L2 error <= 2e-3.
- * Activations must be finite with |x| <= 65504 (the GEMM rounds x to
- * binary16).
+ * Activations must be finite with |x| <= 65504 (the tensor-core paths round
+ * x to binary16).
  * Scratch: the GEMM path needs q4_0_matmul_workspace_bytes(M, N, K) bytes;
  * this entry point takes them with cudaMallocAsync on `stream` and frees
  * them with cudaFreeAsync on the same stream.  Use q4_0_matmul_ws to supply

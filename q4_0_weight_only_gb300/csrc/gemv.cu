@@ -656,6 +656,9 @@ cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t 
         e = M == 1 ? dp::launch<1>(x, wq, y, M, N, K, sms, s, err, &done)
                    : dp::launch<2>(x, wq, y, M, N, K, sms, s, err, &done);
         if (e != cudaSuccess || done) return e;
+    } else {
+        // three or more rows of x: the dot product moves to the tensor cores
+        return launch_gemv_tc(x, wq, y, M, N, K, s, err);
     }
     // rows of x per launch: the largest power of two <= 8 that covers M (or
     // fits shared memory); each launch streams the weights once

@@ -1,0 +1,370 @@
+// gemv_tc.cu -- batched decode (3 <= M <= 32) on the 5th-generation tensor
+// cores.
+//
+// "Vertical disaggregation: maximizing model throughput on heterogeneous
+// silicon", section "Every cycle counts: custom kernels" lists batch decode
+// (several sessions sharing one pass over the weights) among the Q4_0
+// kernels.  With M rows of x, CUDA-core FMAs cannot keep up with the weight
+// stream once M reaches a few rows, so the dot product moves to tcgen05:
+//
+//   * A = dequantised weights, 128 rows x 64 k per stage, in tensor memory
+//     (binary16, d * (q - 8) rounded once), written by eight dequant warps;
+//   * B = x: two warps load bf16 x with plain 16-byte loads (x is small and
+//     L2-resident; tensor copies of it would queue behind the weight stream),
+//     round to binary16 and write the 128-byte-swizzled K-major layout the
+//     MMA reads -- no scratch buffer;
+//   * D = 128 x TM fp32 in tensor memory (TM = 16 or 32, padded rows of x are
+//     zero);
+//   * N is tiled by 128 rows; K is split over the CTAs of a thread-block
+//     cluster (up to 8), each streaming its K range once, and the partial
+//     tiles are summed through distributed shared memory in rank order
+//     (deterministic, no atomics, no global scratch).
+// Waits are bounded; every thread reaches both cluster barriers even when a
+// wait gives up.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <mutex>
+
+#include "q4_0_internal.h"
+#include "q4_0_ptx.cuh"
+
+namespace q4_0 {
+namespace {
+
+constexpr int kTileN = 128;               // weight rows per CTA (MMA M)
+constexpr int kKB = 64;                   // k per MMA stage
+constexpr int kKW = 256;                  // k per weight stage
+constexpr int kWRowBytes = kKW / 32 * 18;  // 144
+constexpr int kWStageBytes = kTileN * kWRowBytes;
+constexpr int kNW = 3, kNX = 2, kNA = 7;  // 32 + 7 x 32 TMEM columns = 256
+constexpr int kDequantWarps = 8;
+constexpr int kConvertWarps = 2;
+constexpr int kThreads = 32 * (2 + kDequantWarps + kConvertWarps);  // 384
+constexpr int kMaxCluster = 8;
+
+__host__ __device__ constexpr uint32_t cols_pow2(uint32_t v) {
+    uint32_t p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+template <int TM>
+struct Cfg {
+    static constexpr uint32_t kXAtom = TM * 128;             // [TM x 64 k] fp16, 128-byte swizzle
+    static constexpr uint32_t kXStage = kXAtom * (kKW / kKB);  // one weight stage of k
+    static constexpr uint32_t kDCols = 32;
+    static constexpr uint32_t kCols = cols_pow2(kDCols + kNA * 32);
+    static constexpr int kPartStride = TM + 1;  // floats per row of the partial tile
+    static constexpr size_t kOffW = (size_t)kNX * kXStage;
+    static constexpr size_t kOffPart = kOffW + (size_t)kNW * kWStageBytes;
+    static constexpr size_t kOffBars = kOffPart + (size_t)kTileN * kPartStride * 4;
+    static constexpr int kNumBars = 2 * kNW + 2 * kNX + 2 * kNA + 2;
+    static constexpr size_t kSmem = 1024 + kOffBars + kNumBars * 8 + 16;
+};
+
+__device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
+__device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// One Q4_0 block -> 16 TMEM columns: column c holds elements (2c, 2c+1).
+__device__ __forceinline__ void dequant_block16(uint32_t dbits, const uint32_t (&Q)[4],
+                                                uint32_t (&out)[16]) {
+    const uint32_t kMagic = 0x64006400u;  // two fp16 1024.0
+    const half2 k1032 = __floats2half2_rn(1032.0f, 1032.0f);
+    const half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits));
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        const uint32_t b01 = __byte_perm(Q[wi], 0u, 0x4140);  // [qs0, 0, qs1, 0]
+        const uint32_t b23 = __byte_perm(Q[wi], 0u, 0x4342);  // [qs2, 0, qs3, 0]
+        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((b01 & 0x000F000Fu) | kMagic), k1032), d2));
+        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((b23 & 0x000F000Fu) | kMagic), k1032), d2));
+        out[8 + 2 * wi + 0] =
+            h2u(__hmul2(__hsub2(u2h(((b01 >> 4) & 0x000F000Fu) | kMagic), k1032), d2));
+        out[8 + 2 * wi + 1] =
+            h2u(__hmul2(__hsub2(u2h(((b23 >> 4) & 0x000F000Fu) | kMagic), k1032), d2));
+    }
+}
+
+template <int TM>
+__global__ void __launch_bounds__(kThreads, 2)
+    gemv_tc_kernel(const uint16_t *__restrict__ x, const __grid_constant__ CUtensorMap wmap,
+                   float *__restrict__ y, int M, int N, int K, unsigned int *err) {
+    using C = Cfg<TM>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *xring = smem;
+    uint8_t *wring = smem + C::kOffW;
+    float *part = reinterpret_cast<float *>(smem + C::kOffPart);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);
+    uint64_t *w_full = bars, *w_empty = bars + kNW;
+    uint64_t *x_conv = bars + 2 * kNW, *x_empty = x_conv + kNX;
+    uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNA;
+    uint64_t *d_full = a_empty + kNA, *drain = d_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = gridDim.x;                 // CTAs of the cluster, along K
+    const int rank = (int)cluster_rank();
+    const int n0 = blockIdx.y * kTileN;
+    const int KU = K / kKW;
+    const int u0 = rank * KU / S, u1 = (rank + 1) * KU / S;
+    const int nW = u1 - u0, nS = nW * (kKW / kKB);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNW; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&w_empty[i], 32 * kDequantWarps);
+        }
+        for (int i = 0; i < kNX; ++i) {
+            mbar_init(&x_conv[i], 32 * kConvertWarps);
+            mbar_init(&x_empty[i], 1);
+        }
+        for (int i = 0; i < kNA; ++i) {
+            mbar_init(&a_full[i], 32 * kDequantWarps / 2);  // one half of the dequant warps
+            mbar_init(&a_empty[i], 1);
+        }
+        mbar_init(d_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&wmap);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::kCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_launch_dependents();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t d_tmem = tmem, a_tmem = tmem + C::kDCols;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // weight stream (weights may be fetched before the previous kernel
+            // ends; x is fetched by the converter warps after pdl_wait)
+            const uint64_t policy = l2_evict_first_policy();  // weights are read once
+            int issued_w = 0;
+            for (int ws = 0; ws < nW; ++ws) {
+                const int wsl = ws % kNW;
+                if (!mbar_wait(&w_empty[wsl], ((ws / kNW) & 1) ^ 1, abort_flag, err)) break;
+                mbar_arrive_expect_tx(&w_full[wsl], kWStageBytes);
+                tma_load_2d_hint(wring + wsl * kWStageBytes, &wmap, (u0 + ws) * kWRowBytes, n0, &w_full[wsl],
+                                 policy);
+                ++issued_w;
+            }
+            for (int i = issued_w - kNW; i < issued_w; ++i)
+                if (i >= 0) mbar_drain(&w_full[i % kNW], (i / kNW) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(kTileN, TM);
+            for (int s = 0; s < nS; ++s) {
+                const int ws = s / (kKW / kKB), sub = s % (kKW / kKB);
+                const int xsl = ws % kNX, asl = s % kNA;
+                if (sub == 0 && !mbar_wait(&x_conv[xsl], (ws / kNX) & 1, abort_flag, err)) break;
+                if (!mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err)) break;
+                tc_fence_after();
+                const uint64_t bdesc = smem_desc_k128(xring + xsl * C::kXStage + sub * C::kXAtom);
+#pragma unroll
+                for (int kk = 0; kk < kKB / 16; ++kk)
+                    mma_f16_ts(d_tmem, a_tmem + asl * 32 + kk * 8, bdesc + 2 * kk, idesc, (s | kk) != 0);
+                mma_commit(&a_empty[asl]);
+                if (sub == kKW / kKB - 1) mma_commit(&x_empty[xsl]);
+            }
+            mma_commit(d_full);
+        }
+    } else if (warp < 2 + kDequantWarps) {
+        // dequant: warp (quarter q, half h) writes 64-k stages 2h and 2h+1 of
+        // every weight stage (both blocks of each, 32 TMEM columns) for the 32
+        // weight rows of its lane quarter; one wait for both stores
+        const int quad = warp & 3, half = (warp - 2) >> 2;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        bool ok = true;
+        for (int ws = 0; ws < nW && ok; ++ws) {
+            const int wsl = ws % kNW;
+            ok = __all_sync(0xffffffffu, mbar_wait(&w_full[wsl], (ws / kNW) & 1, abort_flag, err));
+            if (!ok) break;
+            const uint8_t *row = wring + wsl * kWStageBytes + r * kWRowBytes;
+            const int s0 = ws * (kKW / kKB) + 2 * half;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int s = s0 + j, asl = s % kNA;
+                ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(row + (2 * half + j) * 36);
+                uint32_t wv[9];
+#pragma unroll
+                for (int i = 0; i < 9; ++i) wv[i] = src[i];
+                const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
+                                        __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
+                const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+                uint32_t cols[32];
+                uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols);
+                uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols + 16);
+                dequant_block16(wv[0] & 0xFFFFu, Q0, lo);
+                dequant_block16(wv[4] >> 16, Q1, hi);
+                tmem_st32(a_tmem + lane_base + asl * 32, cols);
+            }
+            if (!ok) break;
+            tmem_wait_st();
+            tc_fence_before();
+#pragma unroll
+            for (int j = 0; j < 2; ++j) mbar_arrive(&a_full[(s0 + j) % kNA]);
+            mbar_arrive(&w_empty[wsl]);
+        }
+        // epilogue (warps 2..5 cover the four lane quarters): D -> partial tile
+        if (half == 0) {
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));
+            if (ok) {
+                tc_fence_after();
+                uint32_t v[16];
+#pragma unroll
+                for (int c = 0; c < TM; c += 16) {
+                    tmem_ld16(d_tmem + lane_base + c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) part[r * C::kPartStride + c + j] = __uint_as_float(v[j]);
+                }
+            }
+        }
+    } else {
+        // x converters: per weight stage, load x[0:M][k0:k0+256] (bf16, 16 bytes
+        // per load), round to binary16 and store into the four 64-k atoms in
+        // the 128-byte-swizzled layout (16-byte chunk c of row m lands at
+        // chunk c ^ (m & 7)); rows m >= M are zero
+        const int t = threadIdx.x - 32 * (2 + kDequantWarps);
+        constexpr int kChunks = TM * (kKW / 8);                 // 16-byte chunks per stage
+        constexpr int kPer = kChunks / (32 * kConvertWarps);    // per thread
+        pdl_wait();  // x may come from the previous kernel
+        for (int ws = 0; ws < nW; ++ws) {
+            const int xsl = ws % kNX;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xsl], ((ws / kNX) & 1) ^ 1, abort_flag, err));
+            if (!ok) break;
+            const int64_t k0 = (int64_t)(u0 + ws) * kKW;
+            uint4 v[kPer];
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int i = t + j * 32 * kConvertWarps, m = i / (kKW / 8), c = i % (kKW / 8);
+                v[j] = m < M ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)m * K + k0) + c)
+                             : make_uint4(0, 0, 0, 0);
+            }
+            uint8_t *stage = xring + xsl * C::kXStage;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int i = t + j * 32 * kConvertWarps, m = i / (kKW / 8), c = i % (kKW / 8);
+                const uint32_t in[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    o[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16),
+                                                 __uint_as_float(in[h] & 0xFFFF0000u)));
+                const int atom = c >> 3, cc = c & 7;
+                *reinterpret_cast<uint4 *>(stage + atom * C::kXAtom + m * 128 + ((cc ^ (m & 7)) << 4)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&x_conv[xsl]);
+        }
+    }
+
+    // cluster reduction: CTA `rank` sums rows [rank * rpc, ...) of the S
+    // partial tiles in rank order and writes y
+    cluster_sync();
+    {
+        const int rpc = (kTileN + S - 1) / S;
+        const int rb = rank * rpc, re = min(kTileN, rb + rpc);
+        const int nr = max(0, re - rb);
+        for (int e = threadIdx.x; e < nr * TM; e += kThreads) {
+            const int m = e / nr, row = rb + (e - m * nr);
+            const int n = n0 + row;
+            if (m < M && n < N) {
+                float v[kMaxCluster];
+#pragma unroll
+                for (int q = 0; q < kMaxCluster; ++q)
+                    v[q] = q < S ? ld_shared_cluster_f32(map_shared_rank(part + row * C::kPartStride + m, (uint32_t)q))
+                                 : 0.f;
+                float sum = 0.f;
+#pragma unroll
+                for (int q = 0; q < kMaxCluster; ++q) sum += v[q];  // rank order
+                y[(int64_t)m * N + n] = sum;
+            }
+        }
+    }
+    cluster_sync();
+    if (warp == 1) {
+        if (lane == 0) {
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kCols);
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+template <int TM>
+cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+                      cudaStream_t s, unsigned int *err) {
+    using C = Cfg<TM>;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap wmap;
+    {
+        const cuuint64_t rowbytes = (cuuint64_t)(K / 32) * 18;
+        const cuuint64_t dims[2] = {rowbytes, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {rowbytes};
+        const cuuint32_t box[2] = {kWRowBytes, kTileN};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(wq), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_tc_kernel<TM>), (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int sms = device_sm_count(dev);
+    const int64_t tiles = (N + kTileN - 1) / kTileN;
+    const int64_t KU = K / kKW;
+    // split K so that about two CTAs per SM are busy, at most 8 per cluster
+    int64_t S = tiles > 0 ? (2 * (int64_t)sms) / tiles : 1;
+    S = S < 1 ? 1 : (S > kMaxCluster ? kMaxCluster : S);
+    if (S > KU) S = KU;
+    if (tiles > 65535) return cudaErrorInvalidValue;
+    return launch_pdl_cluster(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads),
+                              C::kSmem, s, (unsigned)S, x, wmap, y, (int)M, (int)N, (int)K, err);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+                           int64_t K, cudaStream_t s, unsigned int *err) {
+    if (M <= 16) return launch_tm<16>(x, wq, y, M, N, K, s, err);
+    return launch_tm<32>(x, wq, y, M, N, K, s, err);
+}
+
+}  // namespace q4_0

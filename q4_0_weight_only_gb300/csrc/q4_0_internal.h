@@ -32,6 +32,27 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Actual &&>(args)...);
 }
 
+// As launch_pdl, with a thread-block cluster of `cluster_x` CTAs along x.
+template <typename... Params, typename... Actual>
+cudaError_t launch_pdl_cluster(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t s, unsigned cluster_x, Actual &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Actual &&>(args)...);
+}
+
 // Device error word of the current device (a __device__ variable's address).
 unsigned int *device_error_word();
 
@@ -41,6 +62,11 @@ cudaError_t launch_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, c
 // Decode GEMV for M <= 32 (x, y point at row 0; row strides K and N).
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
                         int64_t K, cudaStream_t s, unsigned int *err);
+
+// Tensor-core decode for 3 <= M <= 32: split-K over a thread-block cluster,
+// no scratch memory.
+cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+                           int64_t K, cudaStream_t s, unsigned int *err);
 
 // tcgen05 GEMM; `x16` is caller scratch of gemm_workspace_bytes(M, K).
 size_t gemm_workspace_bytes(int64_t M, int64_t K);
