@@ -349,52 +349,59 @@ __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-// Block b of x row m (32 bf16 values) -> fixed point, written into the
-// pair record of shared memory.
-__device__ __forceinline__ void convert_block(const uint16_t *__restrict__ xrow, int b,
-                                              uint32_t *__restrict__ rec) {
-    float xv[32];
-    if (xrow) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(xrow + (int64_t)b * 32);
+// Eight elements (part `part` of block b of x row m) -> fixed point, written
+// into the pair record; the four threads of a block (consecutive lanes)
+// agree on the block's exponent and sum through shuffles.  `live` is false
+// for lanes past the end (they still take part in the shuffles).
+__device__ __forceinline__ void convert_part(const uint16_t *__restrict__ xrow, int b, int part,
+                                             bool live, uint32_t *__restrict__ rec) {
+    float xv[8];
+    if (live && xrow) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(xrow + (int64_t)b * 32) + part);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 u = __ldg(src + i);
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                xv[8 * i + 2 * h] = __uint_as_float(w4[h] << 16);
-                xv[8 * i + 2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
-            }
+        for (int h = 0; h < 4; ++h) {
+            xv[2 * h] = __uint_as_float(w4[h] << 16);
+            xv[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) xv[j] = 0.f;
+        for (int j = 0; j < 8; ++j) xv[j] = 0.f;
     }
     float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(xv[j]));
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(xv[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     int e = 0;
     if (amax > 0.f) {
         frexpf(amax, &e);
         e = max(-100, min(127, e));
     }
     const float up = amax > 0.f ? ldexpf(1.0f, 14 - e) : 0.f;
-    const int blk = b & 1;
-    int sum = 0;
+    int X[8], sum = 0;
 #pragma unroll
-    for (int wd = 0; wd < 8; ++wd) {
-        int X[4];
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-            X[bb] = __float2int_rn(xv[4 * wd + bb] * up);
-            sum += X[bb];
-        }
-        // bytes 1 (high) and 0 (low) of the four 16-bit fixed-point values
-        rec[blk * 8 + wd] = __byte_perm(__byte_perm(X[0], X[1], 0x0051), __byte_perm(X[2], X[3], 0x0051), 0x5410);
-        rec[16 + blk * 8 + wd] = __byte_perm(__byte_perm(X[0], X[1], 0x0040), __byte_perm(X[2], X[3], 0x0040), 0x5410);
+    for (int j = 0; j < 8; ++j) {
+        X[j] = __float2int_rn(xv[j] * up);
+        sum += X[j];
     }
-    reinterpret_cast<int *>(rec)[32 + blk] = -8 * sum;
-    reinterpret_cast<float *>(rec)[34 + blk] = amax > 0.f ? ldexpf(1.0f, e - 14) : 0.f;
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    if (!live) return;
+    const int blk = b & 1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int wd = 2 * part + h;  // word: elements 4 wd .. 4 wd + 3
+        const int *Xw = X + 4 * h;
+        // bytes 1 (high) and 0 (low) of the four 16-bit fixed-point values
+        rec[blk * 8 + wd] = __byte_perm(__byte_perm(Xw[0], Xw[1], 0x0051), __byte_perm(Xw[2], Xw[3], 0x0051), 0x5410);
+        rec[16 + blk * 8 + wd] =
+            __byte_perm(__byte_perm(Xw[0], Xw[1], 0x0040), __byte_perm(Xw[2], Xw[3], 0x0040), 0x5410);
+    }
+    if (part == 0) {
+        reinterpret_cast<int *>(rec)[32 + blk] = -8 * sum;
+        reinterpret_cast<float *>(rec)[34 + blk] = amax > 0.f ? ldexpf(1.0f, e - 14) : 0.f;
+    }
 }
 
 // One Q4_0 block against MT rows of x: v[m] += d * 2^(e-14) * T.
@@ -489,10 +496,15 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
     // x -> fixed point in shared memory, once per CTA (overlaps the first copies)
     pdl_wait();
     const int nb = 2 * a.P;
-    for (int t = tid; t < MT * nb; t += a.T) {
-        const int m = t / nb, b = t - m * nb;
-        convert_block(m < a.mrows ? x + (int64_t)m * a.K : nullptr, b,
-                      xsm + ((size_t)m * a.P + (b >> 1)) * kPairWords);
+    const int nparts = 4 * MT * nb;  // four threads per 32-element block
+    for (int t0 = tid - lane; t0 < nparts; t0 += a.T) {  // warp-uniform trip count
+        const int t = t0 + lane;
+        const bool live = t < nparts;
+        const int q = live ? t : nparts - 1;
+        const int blk_id = q >> 2, part = q & 3;
+        const int m = blk_id / nb, b = blk_id - m * nb;
+        convert_part(m < a.mrows ? x + (int64_t)m * a.K : nullptr, b, part, live,
+                     xsm + ((size_t)m * a.P + (b >> 1)) * kPairWords);
     }
     asm volatile("bar.sync 1, %0;" ::"r"(a.T) : "memory");
 
