@@ -46,7 +46,8 @@ def parse():
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=200)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["decode", "batched", "prefill", "sweep"], default="decode")
+    p.add_argument("--workload", choices=["decode", "batched", "prefill", "sweep", "chunked"], default="decode")
+    p.add_argument("--m", type=int, default=None, help="rows of x (overrides the workload's M)")
     p.add_argument("--layers", type=int, default=8, help="resident layer copies (decode/batched)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=2000)
@@ -62,16 +63,13 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def workload_shapes(name):
+def workload_shapes(name, m=None):
+    """M and the four layer shapes of a workload.  chunked: one 256-token
+    prefill chunk and a 16-row decode batch as one M = 272 call per matrix."""
     from q4_0_weight_only_gb300 import synth
-    if name == "decode":
-        M = 1
-    elif name == "batched":
-        M = 16
-    elif name == "prefill":
-        M = 2048
-    else:
-        M = 1
+    M = {"decode": 1, "batched": 16, "prefill": 2048, "sweep": 1, "chunked": 272}[name]
+    if m is not None:
+        M = m
     return M, [(s, synth.SHAPES[s]) for s in SHAPE_ORDER]
 
 
@@ -144,14 +142,19 @@ class ClockSampler:
 # ------------------------------------------------------------ distributed
 
 def dist_setup(gpus):
+    """One process per GPU (torchrun env).  NCCL when CUDA is present, gloo
+    otherwise; the matmul itself exchanges nothing between ranks."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend="gloo")
     return rank, world, local
 
 
@@ -162,11 +165,13 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The slowest rank's value (all ranks get it)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -197,7 +202,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     hbm, tf_burst, tf_sust, peak_kind = peaks()
-    M, shapes = workload_shapes(args.workload)
+    M, shapes = workload_shapes(args.workload, args.m)
     layers = 64 if args.workload == "sweep" else (1 if args.workload == "prefill" else args.layers)
     wq = build_layers(q4, synth, shapes, layers, dev)
     g = torch.Generator(device=dev)
@@ -346,10 +351,12 @@ def run_ours(args, rank, world, local):
 
 
 def workload_name(w, M, layers):
-    return {"decode": f"decode M=1, four 27B-class layer matrices per step, {layers} layer copies",
-            "batched": f"batched decode M={M}, four 27B-class layer matrices per step",
+    return {"decode": f"decode M={M}, four 27B-class layer matrices per step, {layers} layer copies",
+            "batched": f"batched decode M={M}, four 27B-class layer matrices per step, {layers} layer copies",
             "prefill": f"prefill M={M}, four 27B-class layer matrices per step",
-            "sweep": "64-layer decode sweep at M=1 (256 matrices per step)"}[w]
+            "sweep": f"64-layer decode sweep at M={M} (256 matrices per step)",
+            "chunked": f"chunked prefill: 256-token chunk + 16 decode rows as one M={M} call per matrix, "
+                       f"four matrices per step, {layers} layer copies"}[w]
 
 
 def load_traffic(workload):
@@ -406,7 +413,7 @@ def run_reference(args, rank, world, local):
     import oracle
     from q4_0_weight_only_gb300 import synth
     o = oracle.get()
-    M, shapes = workload_shapes(args.workload)
+    M, shapes = workload_shapes(args.workload, args.m)
     warm = max(3, args.warmup)
     total_steps = args.steps + warm
     per_step_budget = min(0.5, 150.0 / total_steps)

@@ -177,6 +177,18 @@ int q4_0_gemm_noalloc(const uint16_t *x, const uint8_t *wq, float *y,
  */
 int q4_0_device_error(int *code);
 
+/*
+ * q4_0_selftest_wait_timeout -- exercise the failure path of the bounded
+ * waits.  Launches one thread that waits on an mbarrier nothing arrives on,
+ * gives up after `limit_us` microseconds (1 .. 1e6), records
+ * Q4_0_ERR_DEVICE_TIMEOUT in the device error word and returns; it traps
+ * nothing and leaves the context usable.  Every pipeline wait of the matmul
+ * kernels fails the same way (after about two seconds).  Read the result with
+ * q4_0_device_error().
+ * Returns Q4_0_OK, Q4_0_ERR_INVALID_ARG or Q4_0_ERR_CUDA.
+ */
+int q4_0_selftest_wait_timeout(int64_t limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

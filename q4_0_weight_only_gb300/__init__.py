@@ -6,8 +6,9 @@ Build it with ``q4_0_weight_only_gb300.build.build()``.
 """
 from ._lib import (ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_INVALID_ARG, ERR_UNSUPPORTED,
                    ERR_WORKSPACE, OK, Q4Error, device_error, gemm, gemv, lib, matmul,
-                   matmul_alloc, quantize, status_string, version, weight_bytes)
+                   matmul_alloc, quantize, selftest_wait_timeout, status_string, version,
+                   weight_bytes)
 
 __all__ = ["quantize", "matmul", "matmul_alloc", "gemv", "gemm", "weight_bytes", "device_error",
-           "version", "status_string", "lib", "Q4Error", "OK", "ERR_INVALID_ARG",
+           "version", "status_string", "lib", "selftest_wait_timeout", "Q4Error", "OK", "ERR_INVALID_ARG",
            "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_DEVICE_TIMEOUT", "ERR_WORKSPACE"]

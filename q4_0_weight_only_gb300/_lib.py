@@ -36,6 +36,7 @@ SIGNATURES = {
     "q4_0_gemm_workspace_bytes": ([_I64, _I64], _SZ),
     "q4_0_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemm_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "q4_0_selftest_wait_timeout": ([_I64, _P], _INT),
     "q4_0_device_error": ([ctypes.POINTER(_INT)], _INT),
 }
 
@@ -192,6 +193,13 @@ def gemm_noalloc(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.T
     _check(lib().q4_0_gemm_noalloc(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
                                    _stream(stream)), "q4_0_gemm_noalloc")
     return out
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> int:
+    """Run the bounded-wait failure self-check and return the device error
+    status it leaves (ERR_DEVICE_TIMEOUT when the path works)."""
+    _check(lib().q4_0_selftest_wait_timeout(int(limit_us), _stream(stream)), "q4_0_selftest_wait_timeout")
+    return device_error()
 
 
 def device_error() -> int:

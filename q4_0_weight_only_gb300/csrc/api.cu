@@ -8,6 +8,7 @@
 
 #include "../../include/q4_0.h"
 #include "q4_0_internal.h"
+#include "q4_0_ptx.cuh"
 
 namespace q4_0 {
 
@@ -16,6 +17,25 @@ namespace q4_0 {
 __device__ unsigned int g_device_error_word;
 
 namespace {
+
+// Self-check of the bounded-wait path: one thread waits on an mbarrier that
+// nothing arrives on, gives up after `limit_ns`, records the timeout in the
+// device error word and returns -- the same path every pipeline wait in this
+// library takes.  No trap, no fault: the context stays usable.
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns, unsigned int *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(&bar, 0)) {
+        if (global_ns() - t0 > limit_ns) {
+            atomicExch(err, kErrWaitTimeout);
+            return;
+        }
+    }
+}
+
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<unsigned int *> g_err_ptr[kMaxDevices];
@@ -177,6 +197,15 @@ int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64
     const cudaError_t fe = cudaFreeAsync(ws, s);
     if (st == Q4_0_OK && fe != cudaSuccess) st = Q4_0_ERR_CUDA;
     return st;
+}
+
+int q4_0_selftest_wait_timeout(int64_t limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 1000000) return Q4_0_ERR_INVALID_ARG;
+    unsigned int *err = device_error_word();
+    if (!err) return Q4_0_ERR_CUDA;
+    wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        (unsigned long long)limit_us * 1000ull, err);
+    return from_cuda(cudaGetLastError());
 }
 
 int q4_0_device_error(int *code) {

@@ -156,3 +156,14 @@ def test_prefill(shape):
         del y
         torch.cuda.empty_cache()
     assert q4.device_error() == 0
+
+
+@pytest.mark.parametrize("shape", ["qkv", "down"])
+def test_chunked_prefill_m272(shape):
+    """A 256-token prefill chunk and a 16-row decode batch as one M = 272 call."""
+    q4 = lib()
+    N, K = synth.SHAPES[shape]
+    wq = oracle.get().quantize(synth.prefill_weights(shape))
+    w, x = synth.small_case(500 + synth.SHAPE_ORDER.index(shape), 272, 8, K, act_outlier_frac=0.01)
+    y = q4.matmul(x_dev(x), wq_dev(wq), N, K)
+    check_sampled(y, x, wq, N, K, seed=272)
