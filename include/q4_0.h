@@ -138,10 +138,13 @@ int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y,
 /*
  * q4_0_gemm -- the tcgen05 prefill kernel alone (what q4_0_matmul runs for
  * M > 32), usable at any M >= 1 for cross-checks.  Workspace as in
- * q4_0_matmul_ws (q4_0_gemm_workspace_bytes(M, K) bytes: x rounded to
- * binary16).
+ * q4_0_matmul_ws: q4_0_gemm_workspace_bytes(M, N, K) bytes on the current
+ * device -- x rounded to binary16 and, when the output tiles alone would
+ * leave SMs idle, fp32 partial tiles of a 2- to 4-way split of K (summed
+ * afterwards in split order, so results stay deterministic).  A workspace
+ * large enough for x alone runs without the split.
  */
-size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t K);
+size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y,
               int64_t M, int64_t N, int64_t K,
               void *workspace, size_t workspace_bytes, void *stream);

@@ -33,7 +33,7 @@ SIGNATURES = {
     "q4_0_matmul_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "q4_0_matmul_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemv": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
-    "q4_0_gemm_workspace_bytes": ([_I64, _I64], _SZ),
+    "q4_0_gemm_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "q4_0_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemm_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "q4_0_selftest_wait_timeout": ([_I64, _P], _INT),
@@ -177,7 +177,7 @@ def gemm(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = 
          workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
     """The tcgen05 kernel alone (any M)."""
     M, out = _mm_args(x, wq, N, K, out)
-    ws, wsb = _workspace(int(lib().q4_0_gemm_workspace_bytes(M, K)), x.device, workspace)
+    ws, wsb = _workspace(int(lib().q4_0_gemm_workspace_bytes(M, N, K)), x.device, workspace)
     _check(lib().q4_0_gemm(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
                            ws.data_ptr(), wsb, _stream(stream)), "q4_0_gemm")
     return out

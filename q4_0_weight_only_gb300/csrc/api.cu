@@ -143,15 +143,23 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
                                      device_error_word()));
 }
 
-size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t K) {
-    if (M < 1 || K < 1) return 0;
-    return gemm_workspace_bytes(M, K);
+namespace {
+// K split of the GEMM on the current device (1 when it cannot be queried).
+int current_splits(int64_t M, int64_t N, int64_t K) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    return gemm_splits(M, N, K, device_sm_count(dev));
+}
+}  // namespace
+
+size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 1) return 0;
+    return gemm_workspace_bytes(M, N, K, current_splits(M, N, K));
 }
 
 size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    (void)N;
     if (M <= 32) return 0;
-    return q4_0_gemm_workspace_bytes(M, K);
+    return q4_0_gemm_workspace_bytes(M, N, K);
 }
 
 int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
@@ -168,12 +176,16 @@ int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t
               void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
-    if (!workspace || workspace_bytes < gemm_workspace_bytes(M, K) ||
+    // split K only if the workspace has room for the partial tiles
+    int splits = current_splits(M, N, K);
+    if (workspace_bytes < gemm_workspace_bytes(M, N, K, splits)) splits = 1;
+    if (!workspace || workspace_bytes < gemm_workspace_bytes(M, N, K, 1) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return Q4_0_ERR_WORKSPACE;
     unsigned int *err = device_error_word();
     if (!err) return Q4_0_ERR_CUDA;
-    return from_cuda(launch_gemm(x, wq, y, M, N, K, workspace, static_cast<cudaStream_t>(stream), err));
+    return from_cuda(
+        launch_gemm(x, wq, y, M, N, K, workspace, splits, static_cast<cudaStream_t>(stream), err));
 }
 
 int q4_0_matmul_ws(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
@@ -190,7 +202,7 @@ int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64
     if (st != Q4_0_OK) return st;
     if (M <= 32) return q4_0_gemv(x, wq, y, M, N, K, stream);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t bytes = gemm_workspace_bytes(M, K);
+    const size_t bytes = q4_0_gemm_workspace_bytes(M, N, K);
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return Q4_0_ERR_CUDA;
     st = q4_0_gemm(x, wq, y, M, N, K, ws, bytes, stream);

@@ -8,7 +8,9 @@
 //     tcgen05 kind::f16 MMA takes A and B of one type and binary16 operand
 //     tiles keep the result well inside the error budget (bf16 weight tiles
 //     would not);
-//   * one CTA computes a 128 (weight rows) x TM (x rows) tile of y^T;
+//   * one CTA computes a 128 (weight rows) x TM (x rows) tile of y^T, TM a
+//     multiple of 16 up to 256 chosen per call so that the M tiles carry the
+//     least padding (M = 272 -> two tiles of 144);
 //     warp 0 streams Q4_0 weight tiles [128 rows x 256 k] (144 bytes per row)
 //     and 128-byte-swizzled x tiles [TM rows x 64 k] with tensor TMA;
 //   * warps 2-5 (one thread per weight row) unpack nibbles, apply the scale
@@ -46,14 +48,18 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
     return p;
 }
 
-template <int TM>
-struct GemmCfg {
-    static constexpr uint32_t kXStage = TM * 128;
-    static constexpr uint32_t kDCols = TM < 32 ? 32 : TM;
-    static constexpr uint32_t kCols = pow2_at_least(kDCols + kNA * 32);
-    static constexpr size_t kBarOff = (size_t)kNX * kXStage + (size_t)kNW * kWStageBytes;
+// Shared-memory and TMEM layout of a CTA for an x tile of `tm` rows.
+struct GemmLayout {
+    uint32_t x_stage, d_cols, cols;
+    size_t bar_off, smem;
+    __host__ __device__ explicit GemmLayout(int tm) {
+        x_stage = (uint32_t)tm * 128;
+        d_cols = tm < 32 ? 32 : (uint32_t)((tm + 31) / 32 * 32);
+        cols = pow2_at_least(d_cols + kNA * 32);
+        bar_off = (size_t)kNX * x_stage + (size_t)kNW * kWStageBytes;
+        smem = 1024 + bar_off + kNumBars * 8 + 16;
+    }
     static constexpr int kNumBars = 2 * kNW + 2 * kNX + 2 * kNA + 2;
-    static constexpr size_t kSmem = 1024 + kBarOff + kNumBars * 8 + 16;
 };
 
 __device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
@@ -76,6 +82,24 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__
     x16[i] = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// y = sum over splits of the partial tiles, in split order (deterministic).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__restrict__ part, float4 *__restrict__ y,
+                                                            int64_t n4, int splits) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4 acc = part[i];
+    for (int z = 1; z < splits; ++z) {
+        const float4 v = part[(int64_t)z * n4 + i];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    y[i] = acc;
+}
+
 // One Q4_0 block -> 16 TMEM columns of packed binary16 pairs: column c
 // holds elements (2c, 2c + 1) of the block, each d * (q - 8) rounded once.
 __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q)[4],
@@ -96,27 +120,33 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
     }
 }
 
-template <int TM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                float *__restrict__ y, int M, int N, int K, unsigned int *err) {
-    using Cfg = GemmCfg<TM>;
+                float *__restrict__ y, float *__restrict__ part, int M, int N, int K, int TM,
+                unsigned int *err) {
+    const GemmLayout Cfg(TM);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *xring = smem;
-    uint8_t *wring = smem + kNX * Cfg::kXStage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
+    uint8_t *wring = smem + kNX * Cfg.x_stage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg.bar_off);
     uint64_t *w_full = bars, *w_empty = bars + kNW;
     uint64_t *x_full = bars + 2 * kNW, *x_empty = x_full + kNX;
     uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNA;
     uint64_t *d_full = a_empty + kNA, *drain = d_full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kNumBars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + GemmLayout::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * TM;
-    const int KS = K / kKB, KWS = K / kKW;
+    // split-K: CTA z of gridDim.z takes weight stages [w_begin, w_end) and,
+    // when split, writes its partial tile to part[z] instead of y
+    const int KW_all = K / kKW;
+    const int w_begin = (int)((int64_t)blockIdx.z * KW_all / gridDim.z);
+    const int w_end = (int)((int64_t)(blockIdx.z + 1) * KW_all / gridDim.z);
+    const int KWS = w_end - w_begin, KS = KWS * (kKW / kKB);
+    float *out = part ? part + (size_t)blockIdx.z * M * N : y;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNW; ++i) {
@@ -138,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&xmap);
         tma_prefetch_desc(&wmap);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, Cfg::kCols);
+    if (warp == 1) tmem_alloc(tmem_slot, Cfg.cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -146,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();  // x16 comes from the previous kernel
     const uint32_t tmem = *tmem_slot;
     const uint32_t d_tmem = tmem;
-    const uint32_t a_tmem = tmem + Cfg::kDCols;
+    const uint32_t a_tmem = tmem + Cfg.d_cols;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -156,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int wsl = ws % kNW;
                 if (!mbar_wait(&w_empty[wsl], ((ws / kNW) & 1) ^ 1, abort_flag, err)) break;
                 mbar_arrive_expect_tx(&w_full[wsl], kWStageBytes);
-                tma_load_2d(wring + wsl * kWStageBytes, &wmap, ws * kWRowBytes, n0, &w_full[wsl]);
+                tma_load_2d(wring + wsl * kWStageBytes, &wmap, (w_begin + ws) * kWRowBytes, n0, &w_full[wsl]);
                 ++issued_w;
                 bool ok = true;
                 for (int sub = 0; sub < kKW / kKB; ++sub) {
@@ -165,8 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&x_full[xsl], Cfg::kXStage);
-                    tma_load_2d(xring + xsl * Cfg::kXStage, &xmap, s * kKB, m0, &x_full[xsl]);
+                    mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
+                    tma_load_2d(xring + xsl * Cfg.x_stage, &xmap, w_begin * (kKW / kKB) * kKB + s * kKB, m0,
+                                &x_full[xsl]);
                     ++issued_x;
                 }
                 if (!ok) break;
@@ -179,13 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(kTileN, TM);
+            const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)TM);
             for (int s = 0; s < KS; ++s) {
                 const int xsl = s % kNX, asl = s % kNA;
                 if (!mbar_wait(&x_full[xsl], (s / kNX) & 1, abort_flag, err)) break;
                 if (!mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err)) break;
                 tc_fence_after();
-                const uint64_t bdesc = smem_desc_k128(xring + xsl * Cfg::kXStage);
+                const uint64_t bdesc = smem_desc_k128(xring + xsl * Cfg.x_stage);
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk)
                     mma_f16_ts(d_tmem, a_tmem + asl * 32 + kk * 8, bdesc + 2 * kk, idesc,
@@ -237,14 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             tc_fence_after();
             const int n = n0 + r;
-            for (int c = 0; c < (int)Cfg::kDCols; c += 32) {
+            for (int c = 0; c < TM; c += 32) {
                 uint32_t v[32];
                 tmem_ld32(d_tmem + lane_base + c, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int m = m0 + c + j;
-                    if (c + j < TM && m < M && n < N) y[(int64_t)m * N + n] = __uint_as_float(v[j]);
+                    if (c + j < TM && m < M && n < N) out[(int64_t)m * N + n] = __uint_as_float(v[j]);
                 }
             }
         }
@@ -258,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, Cfg::kCols);
+        tmem_dealloc(tmem, Cfg.cols);
     }
 }
 
@@ -283,17 +314,16 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int TM>
-cudaError_t launch_tm(const void *x16, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
-                      cudaStream_t s, unsigned int *err) {
-    using Cfg = GemmCfg<TM>;
+cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, float *y, float *part, int64_t M,
+                      int64_t N, int64_t K, cudaStream_t s, unsigned int *err) {
+    const GemmLayout Cfg(TM);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap xmap, wmap;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {kKB, TM};
+        const cuuint32_t box[2] = {kKB, (cuuint32_t)TM};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x16), dims, strides, box,
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -311,32 +341,72 @@ cudaError_t launch_tm(const void *x16, const uint8_t *wq, float *y, int64_t M, i
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_kernel<TM>), (int)Cfg::kSmem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_kernel), (int)Cfg.smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM));
-    return launch_pdl(gemm_kernel<TM>, grid, dim3(kThreads), Cfg::kSmem, s, xmap, wmap, y, (int)M,
-                      (int)N, (int)K, err);
+    const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM), (unsigned)splits);
+    e = launch_pdl(gemm_kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr,
+                   (int)M, (int)N, (int)K, TM, err);
+    if (e != cudaSuccess || splits == 1) return e;
+    const int64_t n4 = M * N / 4;
+    return launch_pdl(splitk_reduce_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, s,
+                      reinterpret_cast<const float4 *>(part), reinterpret_cast<float4 *>(y), n4, splits);
 }
 
 }  // namespace
 
-size_t gemm_workspace_bytes(int64_t M, int64_t K) {
-    return (size_t)(((M * K * 2) + 255) / 256 * 256);
+namespace {
+
+int64_t x16_bytes(int64_t M, int64_t K) { return (M * K * 2 + 255) / 256 * 256; }
+
+int tile_rows(int64_t M) {
+    const int64_t tiles_m = (M + 255) / 256;
+    return (int)(((M + tiles_m - 1) / tiles_m + 15) / 16 * 16);
+}
+
+}  // namespace
+
+// Split K 1..4 ways.  Score of a split = share of the SMs busy over whole
+// waves (one CTA per SM) / (1 + cost of the partial tiles), the cost being
+// their write and read (8 * S * M * N bytes at HBM speed) over the MMA time
+// (2 * M * N * K flops at about 1 PFLOP/s): about 600 * S / K.  Each split
+// keeps at least two weight stages.
+int gemm_splits(int64_t M, int64_t N, int64_t K, int sms) {
+    const int64_t ctas = ((N + kTileN - 1) / kTileN) * ((M + tile_rows(M) - 1) / tile_rows(M));
+    if (sms <= 0 || ctas <= 0 || (M * N) % 4 != 0) return 1;
+    int best = 1;
+    double best_score = 0.0;
+    for (int sp = 1; sp <= 4 && K / kKW >= 2 * sp; ++sp) {
+        const int64_t total = ctas * sp;
+        const int64_t waves = (total + sms - 1) / sms;
+        const double busy = (double)total / (double)(waves * sms);
+        const double score = busy / (1.0 + (sp > 1 ? 600.0 * sp / (double)K : 0.0));
+        if (score > best_score * 1.03) {
+            best_score = score;
+            best = sp;
+        }
+    }
+    return best;
+}
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {
+    size_t b = (size_t)x16_bytes(M, K);
+    if (splits > 1) b += (size_t)splits * (size_t)M * (size_t)N * 4;
+    return b;
 }
 
 cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
-                        int64_t K, void *x16, cudaStream_t s, unsigned int *err) {
+                        int64_t K, void *workspace, int splits, cudaStream_t s, unsigned int *err) {
+    void *x16 = workspace;
+    float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + x16_bytes(M, K));
     const int64_t n8 = M * K / 8;
     const int64_t blocks = (n8 + 255) / 256;
     if (blocks > 0x7FFFFFFF || (M + 15) / 16 > 65535) return cudaErrorInvalidValue;
     cudaError_t e = launch_pdl(x_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
                                reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(x16), n8);
     if (e != cudaSuccess) return e;
-    if (M > 128) return launch_tm<256>(x16, wq, y, M, N, K, s, err);
-    if (M > 64) return launch_tm<128>(x16, wq, y, M, N, K, s, err);
-    if (M > 32) return launch_tm<64>(x16, wq, y, M, N, K, s, err);
-    if (M > 16) return launch_tm<32>(x16, wq, y, M, N, K, s, err);
-    return launch_tm<16>(x16, wq, y, M, N, K, s, err);
+    // fewest M tiles of at most 256 rows, then the smallest multiple of 16
+    // that covers M in that many tiles
+    return launch_tm(tile_rows(M), splits < 1 ? 1 : splits, x16, wq, y, part, M, N, K, s, err);
 }
 
 }  // namespace q4_0

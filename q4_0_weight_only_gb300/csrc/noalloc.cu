@@ -68,13 +68,13 @@ extern "C" int q4_0_gemm_noalloc(const uint16_t *x, const uint8_t *wq, float *y,
         M * N > (1ll << 40))
         return Q4_0_ERR_UNSUPPORTED;
     if (M * K > (int64_t)(Q4_0_NOALLOC_SCRATCH_BYTES / 2) ||
-        q4_0::gemm_workspace_bytes(M, K) > Q4_0_NOALLOC_SCRATCH_BYTES)
+        q4_0::gemm_workspace_bytes(M, N, K, 1) > Q4_0_NOALLOC_SCRATCH_BYTES)
         return Q4_0_ERR_WORKSPACE;
     void *scratch = scratch_for_current_device();
     if (!scratch) return Q4_0_ERR_CUDA;
     unsigned int *err = q4_0::device_error_word();
     if (!err) return Q4_0_ERR_CUDA;
     const cudaError_t e =
-        q4_0::launch_gemm(x, wq, y, M, N, K, scratch, static_cast<cudaStream_t>(stream), err);
+        q4_0::launch_gemm(x, wq, y, M, N, K, scratch, 1, static_cast<cudaStream_t>(stream), err);
     return e == cudaSuccess ? Q4_0_OK : Q4_0_ERR_CUDA;
 }

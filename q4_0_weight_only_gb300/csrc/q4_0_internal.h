@@ -68,9 +68,12 @@ cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t 
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
                            int64_t K, cudaStream_t s, unsigned int *err);
 
-// tcgen05 GEMM; `x16` is caller scratch of gemm_workspace_bytes(M, K).
-size_t gemm_workspace_bytes(int64_t M, int64_t K);
+// tcgen05 GEMM.  `workspace` holds x rounded to binary16 and, when K is
+// split (splits > 1), the fp32 partial tiles: gemm_workspace_bytes(M, N, K,
+// splits) bytes.  gemm_splits picks the split for a device with `sms` SMs.
+int gemm_splits(int64_t M, int64_t N, int64_t K, int sms);
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
 cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
-                        int64_t K, void *x16, cudaStream_t s, unsigned int *err);
+                        int64_t K, void *workspace, int splits, cudaStream_t s, unsigned int *err);
 
 }  // namespace q4_0

@@ -56,7 +56,7 @@ def test_workspace_sizes(lib):
     assert lib.q4_0_matmul_workspace_bytes(1, 5120, 5120) == 0
     assert lib.q4_0_matmul_workspace_bytes(32, 5120, 5120) == 0
     assert lib.q4_0_matmul_workspace_bytes(33, 5120, 5120) == 33 * 5120 * 2
-    assert lib.q4_0_gemm_workspace_bytes(3, 256) % 256 == 0
+    assert lib.q4_0_gemm_workspace_bytes(3, 128, 256) % 256 == 0
 
 
 def test_invalid_arguments_rejected_before_cuda(lib):

@@ -56,6 +56,25 @@ def test_dispatch_matches_kernels_bitwise():
         assert torch.equal(q4.matmul_alloc(xd, wd, 384, 1024), y)
 
 
+def test_gemm_split_k_matches_unsplit():
+    """A workspace with room only for x runs the GEMM unsplit; the default
+    workspace may split K (few output tiles). Both meet the tolerance."""
+    q4 = lib()
+    M, N, K = 272, 384, 5120                       # 3 x 2 output tiles: K gets split
+    x, wq = case(8100, M, N, K)
+    xd, wd = x_dev(x), wq_dev(wq)
+    split = q4.gemm(xd, wd, N, K)
+    ws_x_only = torch.empty(q4.lib().q4_0_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    small = ws_x_only[: (M * K * 2 + 255) // 256 * 256]
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    st = q4.lib().q4_0_gemm(xd.data_ptr(), wd.data_ptr(), y.data_ptr(), M, N, K, small.data_ptr(),
+                            small.numel(), None)
+    assert st == q4.OK
+    check_full(split, x, wq, N, K)
+    check_full(y, x, wq, N, K)
+    assert q4.lib().q4_0_gemm_workspace_bytes(M, N, K) > small.numel()
+
+
 def test_gemv_and_gemm_agree():
     q4 = lib()
     for M in (1, 16, 32):
