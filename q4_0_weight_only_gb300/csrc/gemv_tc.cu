@@ -66,12 +66,37 @@ struct Cfg {
 __device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
 __device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-// One Q4_0 block -> 16 TMEM columns: column c holds elements (2c, 2c+1).
-__device__ __forceinline__ void dequant_block16(uint32_t dbits, const uint32_t (&Q)[4],
-                                                uint32_t (&out)[16]) {
+// One Q4_0 block -> 16 TMEM columns of packed binary16 pairs: column c
+// holds elements (2c, 2c+1), each d * (q - 8) rounded once.  A code byte q
+// (0..15) read as an fp8 e4m3 value is exactly q * 2^-9, so one
+// cvt.rn.f16x2.e4m3x2 yields two exact binary16 codes and one fma with
+// (d * 2^9, -8 d) -- both exact in binary16 -- gives d * (q - 8) with a single
+// rounding.  Blocks with |d| >= 64 (d * 2^9 would overflow binary16) take the
+// exponent-bias route: 1024 + q, minus 1032, times d.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_bytes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)two_bytes));
+    return r;
+}
+
+__device__ __forceinline__ void dequant_block16(uint32_t dbits, const uint32_t (&Q)[4], uint32_t (&out)[16]) {
+    const half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits));
+    if ((dbits & 0x7FFFu) < 0x5400u) {  // |d| < 64
+        const half2 dsc = __hmul2(d2, __floats2half2_rn(512.0f, 512.0f));
+        const half2 c8 = __hmul2(d2, __floats2half2_rn(-8.0f, -8.0f));
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+            const uint32_t lo = Q[wi] & 0x0F0F0F0Fu;         // elements 4wi .. 4wi+3
+            const uint32_t hi = (Q[wi] >> 4) & 0x0F0F0F0Fu;  // elements 16+4wi .. 16+4wi+3
+            out[2 * wi + 0] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(lo & 0xFFFFu)), dsc, c8));
+            out[2 * wi + 1] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(lo >> 16)), dsc, c8));
+            out[8 + 2 * wi + 0] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(hi & 0xFFFFu)), dsc, c8));
+            out[8 + 2 * wi + 1] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(hi >> 16)), dsc, c8));
+        }
+        return;
+    }
     const uint32_t kMagic = 0x64006400u;  // two fp16 1024.0
     const half2 k1032 = __floats2half2_rn(1032.0f, 1032.0f);
-    const half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits));
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
         const uint32_t b01 = __byte_perm(Q[wi], 0u, 0x4140);  // [qs0, 0, qs1, 0]

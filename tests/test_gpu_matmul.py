@@ -75,6 +75,24 @@ def test_gemm_split_k_matches_unsplit():
     assert q4.lib().q4_0_gemm_workspace_bytes(M, N, K) > small.numel()
 
 
+def test_large_scales_take_the_exact_fallback():
+    """Blocks whose scale d reaches |d| >= 64 (|w| up to ~1000) dequantise
+    through the exponent-bias route; mixed with ordinary blocks in one
+    matrix, through the batched decode and the GEMM."""
+    q4 = lib()
+    g = synth.generator(8200)
+    N, K = 300, 2048
+    w = synth.weights(g, N, K)
+    big = g.random((N, K // 32)) < 0.1
+    w.reshape(N, K // 32, 32)[big] *= np.float32(30000.0)     # |d| around 100..300
+    wq = oracle.get().quantize(w)
+    codes, dbits = oracle.get().unpack(wq, N, K)
+    assert ((dbits & 0x7FFF) >= 0x5400).any() and ((dbits & 0x7FFF) < 0x5400).any()
+    for M in (4, 20, 64):
+        x = synth.to_bf16_bits(synth.activations_f32(g, M, K))
+        check_full(q4.matmul(x_dev(x), wq_dev(wq), N, K), x, wq, N, K)
+
+
 def test_gemv_and_gemm_agree():
     q4 = lib()
     for M in (1, 16, 32):
