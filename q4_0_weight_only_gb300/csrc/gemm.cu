@@ -175,14 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNW; ++i) {
             mbar_init(&w_full[i], 1);
-            mbar_init(&w_empty[i], 128);
+            mbar_init(&w_empty[i], 4);  // one arrival per dequant warp
         }
         for (int i = 0; i < kNX; ++i) {
             mbar_init(&x_full[i], 1);
             mbar_init(&x_empty[i], 1);
         }
         for (int i = 0; i < kNA; ++i) {
-            mbar_init(&a_full[i], 128);
+            mbar_init(&a_full[i], 4);
             mbar_init(&a_empty[i], 1);
         }
         mbar_init(d_full, 1);
@@ -233,13 +233,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)TM);
-            for (int s = 0; s < KS; ++s) {
-                const int xsl = s % kNX, asl = s % kNA;
-                if (!mbar_wait(&x_full[xsl], (s / kNX) & 1, abort_flag, err)) break;
-                if (!mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err)) break;
-                tc_fence_after();
+        // MMA issue: the whole warp waits and loops (converged); one elected
+        // lane issues the MMAs and commits
+        const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)TM);
+        for (int s = 0; s < KS; ++s) {
+            const int xsl = s % kNX, asl = s % kNA;
+            if (!__all_sync(0xffffffffu, mbar_wait(&x_full[xsl], (s / kNX) & 1, abort_flag, err))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err))) break;
+            tc_fence_after();
+            if (elect_one()) {
                 const uint64_t bdesc = smem_desc_k128(xring + xsl * Cfg.x_stage);
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk)
@@ -248,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&x_empty[xsl]);
                 mma_commit(&a_empty[asl]);
             }
-            mma_commit(d_full);
+            __syncwarp();
         }
+        if (elect_one()) mma_commit(d_full);
+        __syncwarp();
     } else {
         // warps 2..5: dequantise into TMEM, then the epilogue
         const int quad = warp & 3;
@@ -282,10 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st32(a_tmem + lane_base + asl * 32, cols);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&a_full[asl]);
+                __syncwarp();  // every lane's stores are done
+                if (lane == 0) mbar_arrive(&a_full[asl]);
             }
             if (!ok) break;
-            mbar_arrive(&w_empty[wsl]);
+            __syncwarp();  // every lane's reads of the stage are done
+            if (lane == 0) mbar_arrive(&w_empty[wsl]);
         }
         // epilogue: D[row r][column m] -> y[m][n0 + r]
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));

@@ -140,14 +140,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNW; ++i) {
             mbar_init(&w_full[i], 1);
-            mbar_init(&w_empty[i], 32 * kDequantWarps);
+            mbar_init(&w_empty[i], kDequantWarps);  // one arrival per warp
         }
         for (int i = 0; i < kNX; ++i) {
-            mbar_init(&x_conv[i], 32 * kConvertWarps);
+            mbar_init(&x_conv[i], kConvertWarps);
             mbar_init(&x_empty[i], 1);
         }
         for (int i = 0; i < kNA; ++i) {
-            mbar_init(&a_full[i], 32 * kDequantWarps / 2);  // one half of the dequant warps
+            mbar_init(&a_full[i], kDequantWarps / 2);  // one half of the dequant warps
             mbar_init(&a_empty[i], 1);
         }
         mbar_init(d_full, 1);
@@ -182,14 +182,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (i >= 0) mbar_drain(&w_full[i % kNW], (i / kNW) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(kTileN, TM);
-            for (int s = 0; s < nS; ++s) {
-                const int ws = s / (kKW / kKB), sub = s % (kKW / kKB);
-                const int xsl = ws % kNX, asl = s % kNA;
-                if (sub == 0 && !mbar_wait(&x_conv[xsl], (ws / kNX) & 1, abort_flag, err)) break;
-                if (!mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err)) break;
-                tc_fence_after();
+        // MMA issue: the whole warp waits and loops (converged); one elected
+        // lane issues the MMAs and commits
+        constexpr uint32_t idesc = idesc_f16_f32(kTileN, TM);
+        for (int s = 0; s < nS; ++s) {
+            const int ws = s / (kKW / kKB), sub = s % (kKW / kKB);
+            const int xsl = ws % kNX, asl = s % kNA;
+            if (sub == 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(&x_conv[xsl], (ws / kNX) & 1, abort_flag, err)))
+                break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err))) break;
+            tc_fence_after();
+            if (elect_one()) {
                 const uint64_t bdesc = smem_desc_k128(xring + xsl * C::kXStage + sub * C::kXAtom);
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk)
@@ -197,8 +201,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mma_commit(&a_empty[asl]);
                 if (sub == kKW / kKB - 1) mma_commit(&x_empty[xsl]);
             }
-            mma_commit(d_full);
+            __syncwarp();
         }
+        if (elect_one()) mma_commit(d_full);
+        __syncwarp();
     } else if (warp < 2 + kDequantWarps) {
         // dequant: warp (quarter q, half h) writes 64-k stages 2h and 2h+1 of
         // every weight stage (both blocks of each, 32 TMEM columns) for the 32
@@ -236,9 +242,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!ok) break;
             tmem_wait_st();
             tc_fence_before();
+            __syncwarp();  // every lane's stores (and reads of the stage) are done
+            if (lane == 0) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) mbar_arrive(&a_full[(s0 + j) % kNA]);
-            mbar_arrive(&w_empty[wsl]);
+                for (int j = 0; j < 2; ++j) mbar_arrive(&a_full[(s0 + j) % kNA]);
+                mbar_arrive(&w_empty[wsl]);
+            }
         }
         // epilogue (warps 2..5 cover the four lane quarters): D -> partial tile
         if (half == 0) {
@@ -291,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(&x_conv[xsl]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_conv[xsl]);
         }
     }
 

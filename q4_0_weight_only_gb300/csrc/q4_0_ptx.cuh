@@ -208,6 +208,21 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// True in exactly one lane of a converged warp (the lowest active one, so the
+// same lane every time the whole warp is converged).  The MMA issue loops run
+// on the whole warp and let this lane issue: tcgen05.mma/commit issued from a
+// region where one lane alone is active cost several times more issue cycles
+// per instruction than the same instructions under elect.sync.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
+
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
