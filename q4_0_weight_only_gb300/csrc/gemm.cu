@@ -65,7 +65,17 @@ struct GemmLayout {
 __device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
 __device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-// bf16 -> binary16 (round to nearest even), 8 elements per thread.
+// Swap the middle two binary16 values of each group of four held in the word
+// pair (a, b) = (x0 x1, x2 x3) -> (x0 x2, x1 x3): the k order of the MMA's A
+// tiles (see dequant_block below).
+__device__ __forceinline__ void swap_mid_pairs(uint32_t &a, uint32_t &b) {
+    const uint32_t lo = __byte_perm(a, b, 0x5410), hi = __byte_perm(a, b, 0x7632);
+    a = lo;
+    b = hi;
+}
+
+// bf16 -> binary16 (round to nearest even), 8 elements per thread, in the k
+// order of the weight tiles (middle pair of every group of four swapped).
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__ x,
                                                        uint4 *__restrict__ x16, int64_t n8) {
     pdl_launch_dependents();
@@ -79,6 +89,8 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__
     for (int h = 0; h < 4; ++h)
         out[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16),
                                        __uint_as_float(in[h] & 0xFFFF0000u)));
+    swap_mid_pairs(out[0], out[1]);
+    swap_mid_pairs(out[2], out[3]);
     x16[i] = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
@@ -100,47 +112,40 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__rest
     y[i] = acc;
 }
 
-// One Q4_0 block -> 16 TMEM columns of packed binary16 pairs: column c
-// holds elements (2c, 2c+1), each d * (q - 8) rounded once.  A code byte q
-// (0..15) read as an fp8 e4m3 value is exactly q * 2^-9, so one
-// cvt.rn.f16x2.e4m3x2 yields two exact binary16 codes and one fma with
-// (d * 2^9, -8 d) -- both exact in binary16 -- gives d * (q - 8) with a single
-// rounding.  Blocks with |d| >= 64 (d * 2^9 would overflow binary16) take the
-// exponent-bias route: 1024 + q, minus 1032, times d.
-__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_bytes) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)two_bytes));
-    return r;
-}
-
+// One Q4_0 block -> 16 TMEM columns of packed binary16 pairs, each value
+// d * (q - 8) rounded once.  Exponent-bias decode with no nibble shifts: a
+// low nibble OR-ed into the mantissa of 1024.0 gives 1024 + q, a high nibble
+// masked in place gives 1024 + 16 q (both exact); (v - 1032) * d and
+// (v - 1152) * (d / 16) are then exact small integers times d, rounded once.
+// One 32-bit word of codes yields its bytes 0 and 2 (or 1 and 3) as a pair, so
+// within every aligned group of four elements the pair order is (0, 2), (1, 3):
+// k positions 1 and 2 of each group are swapped, and the x operand carries the
+// same swap (swap_mid_pairs).  d / 16 is exact for |d| >= 2^-10; smaller scales
+// shift the high nibbles down and use the 1032 route for them too.  The shift
+// by a byte is a high multiply, which runs on the FMA pipe rather than the ALU.
 __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q)[4], uint32_t *out) {
-    const half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits));
-    if ((dbits & 0x7FFFu) < 0x5400u) {  // |d| < 64
-        const half2 dsc = __hmul2(d2, __floats2half2_rn(512.0f, 512.0f));
-        const half2 c8 = __hmul2(d2, __floats2half2_rn(-8.0f, -8.0f));
+    const uint32_t kBias = 0x64006400u;                         // (1024, 1024)
+    const half2 k1032 = u2h(0x64086408u), k1152 = u2h(0x64806480u);
+    const half2 d2 = u2h(dbits * 0x00010001u);                  // (d, d)
+    if ((dbits & 0x7C00u) >= 0x1400u) {                         // |d| >= 2^-10
+        const half2 d16 = __hmul2(d2, u2h(0x2C002C00u));         // d / 16, exact
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
-            const uint32_t lo = Q[wi] & 0x0F0F0F0Fu;         // elements 4wi .. 4wi+3
-            const uint32_t hi = (Q[wi] >> 4) & 0x0F0F0F0Fu;  // elements 16+4wi .. 16+4wi+3
-            out[2 * wi + 0] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(lo & 0xFFFFu)), dsc, c8));
-            out[2 * wi + 1] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(lo >> 16)), dsc, c8));
-            out[8 + 2 * wi + 0] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(hi & 0xFFFFu)), dsc, c8));
-            out[8 + 2 * wi + 1] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(hi >> 16)), dsc, c8));
+            const uint32_t q = Q[wi], t = __umulhi(q, 1u << 24);  // t = q >> 8
+            out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x000F000Fu) | kBias), k1032), d2));
+            out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x000F000Fu) | kBias), k1032), d2));
+            out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x00F000F0u) | kBias), k1152), d16));
+            out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x00F000F0u) | kBias), k1152), d16));
         }
         return;
     }
-    const uint32_t kMagic = 0x64006400u;  // two fp16 1024.0
-    const half2 k1032 = __floats2half2_rn(1032.0f, 1032.0f);
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
-        const uint32_t b01 = __byte_perm(Q[wi], 0u, 0x4140);  // [qs0, 0, qs1, 0]
-        const uint32_t b23 = __byte_perm(Q[wi], 0u, 0x4342);  // [qs2, 0, qs3, 0]
-        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((b01 & 0x000F000Fu) | kMagic), k1032), d2));
-        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((b23 & 0x000F000Fu) | kMagic), k1032), d2));
-        out[8 + 2 * wi + 0] =
-            h2u(__hmul2(__hsub2(u2h(((b01 >> 4) & 0x000F000Fu) | kMagic), k1032), d2));
-        out[8 + 2 * wi + 1] =
-            h2u(__hmul2(__hsub2(u2h(((b23 >> 4) & 0x000F000Fu) | kMagic), k1032), d2));
+        const uint32_t q = Q[wi], t = q >> 8;
+        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x000F000Fu) | kBias), k1032), d2));
+        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x000F000Fu) | kBias), k1032), d2));
+        out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(((q >> 4) & 0x000F000Fu) | kBias), k1032), d2));
+        out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(((t >> 4) & 0x000F000Fu) | kBias), k1032), d2));
     }
 }
 
@@ -264,17 +269,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int wsl = ws % kNW;
             ok = __all_sync(0xffffffffu, mbar_wait(&w_full[wsl], (ws / kNW) & 1, abort_flag, err));
             if (!ok) break;
-            const uint8_t *row = wring + wsl * kWStageBytes + r * kWRowBytes;
+            // the row's 144 bytes with nine 16-byte loads: with a 144-byte row
+            // stride the eight lanes of each load phase hit distinct 16-byte
+            // bank groups (4-byte loads would conflict four ways).  The stage
+            // is free again once every lane holds its row.
+            const uint4 *row = reinterpret_cast<const uint4 *>(wring + wsl * kWStageBytes + r * kWRowBytes);
+            uint32_t rw[36];
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+                const uint4 q = row[i];
+                rw[4 * i + 0] = q.x;
+                rw[4 * i + 1] = q.y;
+                rw[4 * i + 2] = q.z;
+                rw[4 * i + 3] = q.w;
+            }
+            __syncwarp();  // every lane's reads of the stage are done
+            if (lane == 0) mbar_arrive(&w_empty[wsl]);
+#pragma unroll
             for (int sub = 0; sub < kKW / kKB; ++sub) {
                 const int s = ws * (kKW / kKB) + sub, asl = s % kNA;
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t *src = reinterpret_cast<const uint32_t *>(row + sub * 36);
-                uint32_t wv[9];
-#pragma unroll
-                for (int i = 0; i < 9; ++i) wv[i] = src[i];
+                const uint32_t *wv = rw + 9 * sub;
                 const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16),
                                         __funnelshift_r(wv[1], wv[2], 16),
                                         __funnelshift_r(wv[2], wv[3], 16),
@@ -289,9 +307,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();  // every lane's stores are done
                 if (lane == 0) mbar_arrive(&a_full[asl]);
             }
-            if (!ok) break;
-            __syncwarp();  // every lane's reads of the stage are done
-            if (lane == 0) mbar_arrive(&w_empty[wsl]);
         }
         // epilogue: D[row r][column m] -> y[m][n0 + r]
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));

@@ -7,8 +7,11 @@
 // kernels.  With M rows of x, CUDA-core FMAs cannot keep up with the weight
 // stream once M reaches a few rows, so the dot product moves to tcgen05:
 //
-//   * A = dequantised weights, 128 rows x 64 k per stage, in tensor memory
+//   * A = dequantised weights, 128 rows x 128 k per slot, in tensor memory
 //     (binary16, d * (q - 8) rounded once), written by eight dequant warps;
+//     one MMA-warp iteration issues the slot's eight MMAs (the issuing warp
+//     shares its scheduler with the dequant warps, so fewer, larger
+//     iterations keep it off the critical path);
 //   * B = x: two warps load bf16 x with plain 16-byte loads (x is small and
 //     L2-resident; tensor copies of it would queue behind the weight stream),
 //     round to binary16 and write the 128-byte-swizzled K-major layout the
@@ -33,11 +36,12 @@ namespace q4_0 {
 namespace {
 
 constexpr int kTileN = 128;               // weight rows per CTA (MMA M)
-constexpr int kKB = 64;                   // k per MMA stage
+constexpr int kKB = 128;                  // k per A slot (one MMA-warp iteration: 8 MMAs)
 constexpr int kKW = 256;                  // k per weight stage
+constexpr int kSubs = kKW / kKB;          // A slots per weight stage
 constexpr int kWRowBytes = kKW / 32 * 18;  // 144
 constexpr int kWStageBytes = kTileN * kWRowBytes;
-constexpr int kNW = 3, kNX = 2, kNA = 7;  // 32 + 7 x 32 TMEM columns = 256
+constexpr int kNW = 3, kNX = 2, kNA = 3;  // 32 + 3 x 64 TMEM columns <= 256
 constexpr int kDequantWarps = 8;
 constexpr int kConvertWarps = 2;
 constexpr int kThreads = 32 * (2 + kDequantWarps + kConvertWarps);  // 384
@@ -52,9 +56,9 @@ __host__ __device__ constexpr uint32_t cols_pow2(uint32_t v) {
 template <int TM>
 struct Cfg {
     static constexpr uint32_t kXAtom = TM * 128;             // [TM x 64 k] fp16, 128-byte swizzle
-    static constexpr uint32_t kXStage = kXAtom * (kKW / kKB);  // one weight stage of k
+    static constexpr uint32_t kXStage = kXAtom * (kKW / 64);   // one weight stage of k
     static constexpr uint32_t kDCols = 32;
-    static constexpr uint32_t kCols = cols_pow2(kDCols + kNA * 32);
+    static constexpr uint32_t kCols = cols_pow2(kDCols + kNA * (kKB / 2));
     static constexpr int kPartStride = TM + 1;  // floats per row of the partial tile
     static constexpr size_t kOffW = (size_t)kNX * kXStage;
     static constexpr size_t kOffPart = kOffW + (size_t)kNW * kWStageBytes;
@@ -66,48 +70,50 @@ struct Cfg {
 __device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
 __device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
-// One Q4_0 block -> 16 TMEM columns of packed binary16 pairs: column c
-// holds elements (2c, 2c+1), each d * (q - 8) rounded once.  A code byte q
-// (0..15) read as an fp8 e4m3 value is exactly q * 2^-9, so one
-// cvt.rn.f16x2.e4m3x2 yields two exact binary16 codes and one fma with
-// (d * 2^9, -8 d) -- both exact in binary16 -- gives d * (q - 8) with a single
-// rounding.  Blocks with |d| >= 64 (d * 2^9 would overflow binary16) take the
-// exponent-bias route: 1024 + q, minus 1032, times d.
-__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_bytes) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)two_bytes));
-    return r;
-}
-
+// One Q4_0 block -> 16 TMEM columns of packed binary16 pairs, each value
+// d * (q - 8) rounded once.  Exponent-bias decode with no nibble shifts: a
+// low nibble OR-ed into the mantissa of 1024.0 gives 1024 + q, a high nibble
+// masked in place gives 1024 + 16 q (both exact); (v - 1032) * d and
+// (v - 1152) * (d / 16) are then exact small integers times d, rounded once.
+// One 32-bit word of codes yields its bytes 0 and 2 (or 1 and 3) as a pair, so
+// within every aligned group of four elements the pair order is (0, 2), (1, 3):
+// k positions 1 and 2 of each group are swapped, and the x operand carries the
+// same swap (swap_mid_pairs).  d / 16 is exact for |d| >= 2^-10; smaller scales
+// shift the high nibbles down and use the 1032 route for them too.  The shift
+// by a byte is a high multiply, which runs on the FMA pipe rather than the ALU.
 __device__ __forceinline__ void dequant_block16(uint32_t dbits, const uint32_t (&Q)[4], uint32_t (&out)[16]) {
-    const half2 d2 = __half2half2(__ushort_as_half((unsigned short)dbits));
-    if ((dbits & 0x7FFFu) < 0x5400u) {  // |d| < 64
-        const half2 dsc = __hmul2(d2, __floats2half2_rn(512.0f, 512.0f));
-        const half2 c8 = __hmul2(d2, __floats2half2_rn(-8.0f, -8.0f));
+    const uint32_t kBias = 0x64006400u;                         // (1024, 1024)
+    const half2 k1032 = u2h(0x64086408u), k1152 = u2h(0x64806480u);
+    const half2 d2 = u2h(dbits * 0x00010001u);                  // (d, d)
+    if ((dbits & 0x7C00u) >= 0x1400u) {                         // |d| >= 2^-10
+        const half2 d16 = __hmul2(d2, u2h(0x2C002C00u));         // d / 16, exact
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
-            const uint32_t lo = Q[wi] & 0x0F0F0F0Fu;         // elements 4wi .. 4wi+3
-            const uint32_t hi = (Q[wi] >> 4) & 0x0F0F0F0Fu;  // elements 16+4wi .. 16+4wi+3
-            out[2 * wi + 0] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(lo & 0xFFFFu)), dsc, c8));
-            out[2 * wi + 1] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(lo >> 16)), dsc, c8));
-            out[8 + 2 * wi + 0] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(hi & 0xFFFFu)), dsc, c8));
-            out[8 + 2 * wi + 1] = h2u(__hfma2(u2h(cvt_e4m3x2_f16x2(hi >> 16)), dsc, c8));
+            const uint32_t q = Q[wi], t = __umulhi(q, 1u << 24);  // t = q >> 8
+            out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x000F000Fu) | kBias), k1032), d2));
+            out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x000F000Fu) | kBias), k1032), d2));
+            out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x00F000F0u) | kBias), k1152), d16));
+            out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x00F000F0u) | kBias), k1152), d16));
         }
         return;
     }
-    const uint32_t kMagic = 0x64006400u;  // two fp16 1024.0
-    const half2 k1032 = __floats2half2_rn(1032.0f, 1032.0f);
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
-        const uint32_t b01 = __byte_perm(Q[wi], 0u, 0x4140);  // [qs0, 0, qs1, 0]
-        const uint32_t b23 = __byte_perm(Q[wi], 0u, 0x4342);  // [qs2, 0, qs3, 0]
-        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((b01 & 0x000F000Fu) | kMagic), k1032), d2));
-        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((b23 & 0x000F000Fu) | kMagic), k1032), d2));
-        out[8 + 2 * wi + 0] =
-            h2u(__hmul2(__hsub2(u2h(((b01 >> 4) & 0x000F000Fu) | kMagic), k1032), d2));
-        out[8 + 2 * wi + 1] =
-            h2u(__hmul2(__hsub2(u2h(((b23 >> 4) & 0x000F000Fu) | kMagic), k1032), d2));
+        const uint32_t q = Q[wi], t = q >> 8;
+        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x000F000Fu) | kBias), k1032), d2));
+        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x000F000Fu) | kBias), k1032), d2));
+        out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(((q >> 4) & 0x000F000Fu) | kBias), k1032), d2));
+        out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(((t >> 4) & 0x000F000Fu) | kBias), k1032), d2));
     }
+}
+
+// Swap the middle two binary16 values of each group of four held in the word
+// pair (a, b) = (x0 x1, x2 x3) -> (x0 x2, x1 x3): the k order of the MMA's A
+// tiles (see the dequantisation above).
+__device__ __forceinline__ void swap_mid_pairs(uint32_t &a, uint32_t &b) {
+    const uint32_t lo = __byte_perm(a, b, 0x5410), hi = __byte_perm(a, b, 0x7632);
+    a = lo;
+    b = hi;
 }
 
 template <int TM>
@@ -135,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int n0 = blockIdx.y * kTileN;
     const int KU = K / kKW;
     const int u0 = rank * KU / S, u1 = (rank + 1) * KU / S;
-    const int nW = u1 - u0, nS = nW * (kKW / kKB);
+    const int nW = u1 - u0, nS = nW * kSubs;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNW; ++i) {
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // lane issues the MMAs and commits
         constexpr uint32_t idesc = idesc_f16_f32(kTileN, TM);
         for (int s = 0; s < nS; ++s) {
-            const int ws = s / (kKW / kKB), sub = s % (kKW / kKB);
+            const int ws = s / kSubs, sub = s % kSubs;
             const int xsl = ws % kNX, asl = s % kNA;
             if (sub == 0 &&
                 !__all_sync(0xffffffffu, mbar_wait(&x_conv[xsl], (ws / kNX) & 1, abort_flag, err)))
@@ -194,21 +200,24 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err))) break;
             tc_fence_after();
             if (elect_one()) {
-                const uint64_t bdesc = smem_desc_k128(xring + xsl * C::kXStage + sub * C::kXAtom);
+                // x atoms of 64 k are contiguous: the descriptor's start address
+                // moves by one atom every four MMAs
+                const uint64_t bdesc = smem_desc_k128(xring + xsl * C::kXStage + sub * (kKB / 64) * C::kXAtom);
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk)
-                    mma_f16_ts(d_tmem, a_tmem + asl * 32 + kk * 8, bdesc + 2 * kk, idesc, (s | kk) != 0);
+                    mma_f16_ts(d_tmem, a_tmem + asl * (kKB / 2) + kk * 8,
+                               bdesc + (kk / 4) * (C::kXAtom >> 4) + 2 * (kk % 4), idesc, (s | kk) != 0);
                 mma_commit(&a_empty[asl]);
-                if (sub == kKW / kKB - 1) mma_commit(&x_empty[xsl]);
+                if (sub == kSubs - 1) mma_commit(&x_empty[xsl]);
             }
             __syncwarp();
         }
         if (elect_one()) mma_commit(d_full);
         __syncwarp();
     } else if (warp < 2 + kDequantWarps) {
-        // dequant: warp (quarter q, half h) writes 64-k stages 2h and 2h+1 of
-        // every weight stage (both blocks of each, 32 TMEM columns) for the 32
-        // weight rows of its lane quarter; one wait for both stores
+        // dequant: warp (quarter q, half h) writes the A slot of k half h of
+        // every weight stage (four blocks, 64 TMEM columns) for the 32 weight
+        // rows of its lane quarter; one wait for both stores
         const int quad = warp & 3, half = (warp - 2) >> 2;
         const int r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -217,18 +226,35 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int wsl = ws % kNW;
             ok = __all_sync(0xffffffffu, mbar_wait(&w_full[wsl], (ws / kNW) & 1, abort_flag, err));
             if (!ok) break;
-            const uint8_t *row = wring + wsl * kWStageBytes + r * kWRowBytes;
-            const int s0 = ws * (kKW / kKB) + 2 * half;
+            // this warp's half of the row (bytes 72h .. 72h + 71) with five
+            // 16-byte loads from byte 64h: a 144-byte row stride puts the eight
+            // lanes of each load phase on distinct 16-byte bank groups, where
+            // 4-byte loads would conflict four ways; half 1 drops the first two
+            // words (warp-uniform selects keep every register index static)
+            const uint4 *row = reinterpret_cast<const uint4 *>(wring + wsl * kWStageBytes + r * kWRowBytes + 64 * half);
+            uint32_t rw[20];
+#pragma unroll
+            for (int i = 0; i < 5; ++i) {
+                const uint4 q = row[i];
+                rw[4 * i + 0] = q.x;
+                rw[4 * i + 1] = q.y;
+                rw[4 * i + 2] = q.z;
+                rw[4 * i + 3] = q.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 18; ++i) rw[i] = half ? rw[i + 2] : rw[i];
+            __syncwarp();  // every lane holds its part of the stage: release it
+            if (lane == 0) mbar_arrive(&w_empty[wsl]);
+            // A slot s = (stage, half): 128 k = two 64-k pieces of 32 columns
+            const int s = ws * kSubs + half, asl = s % kNA;
+            ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int s = s0 + j, asl = s % kNA;
-                ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t *src = reinterpret_cast<const uint32_t *>(row + (2 * half + j) * 36);
                 uint32_t wv[9];
 #pragma unroll
-                for (int i = 0; i < 9; ++i) wv[i] = src[i];
+                for (int i = 0; i < 9; ++i) wv[i] = rw[9 * j + i];
                 const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
                                         __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
                 const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
@@ -237,17 +263,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols + 16);
                 dequant_block16(wv[0] & 0xFFFFu, Q0, lo);
                 dequant_block16(wv[4] >> 16, Q1, hi);
-                tmem_st32(a_tmem + lane_base + asl * 32, cols);
+                tmem_st32(a_tmem + lane_base + asl * (kKB / 2) + j * 32, cols);
             }
-            if (!ok) break;
             tmem_wait_st();
             tc_fence_before();
-            __syncwarp();  // every lane's stores (and reads of the stage) are done
-            if (lane == 0) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j) mbar_arrive(&a_full[(s0 + j) % kNA]);
-                mbar_arrive(&w_empty[wsl]);
-            }
+            __syncwarp();  // every lane's stores are done
+            if (lane == 0) mbar_arrive(&a_full[asl]);
         }
         // epilogue (warps 2..5 cover the four lane quarters): D -> partial tile
         if (half == 0) {
@@ -295,6 +316,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int h = 0; h < 4; ++h)
                     o[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16),
                                                  __uint_as_float(in[h] & 0xFFFF0000u)));
+                swap_mid_pairs(o[0], o[1]);  // the k order of the weight tiles
+                swap_mid_pairs(o[2], o[3]);
                 const int atom = c >> 3, cc = c & 7;
                 *reinterpret_cast<uint4 *>(stage + atom * C::kXAtom + m * 128 + ((cc ^ (m & 7)) << 4)) =
                     make_uint4(o[0], o[1], o[2], o[3]);

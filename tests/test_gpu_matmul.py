@@ -93,6 +93,28 @@ def test_large_scales_take_the_exact_fallback():
         check_full(q4.matmul(x_dev(x), wq_dev(wq), N, K), x, wq, N, K)
 
 
+def test_small_scales_take_the_shift_route():
+    """Every block with |d| < 2^-10 (normal, subnormal and zero scales): the
+    tensor-core dequantisation cannot use d / 16 there and shifts the high
+    nibbles instead.  All blocks are small, so an error in that route is not
+    hidden by larger blocks in the error budget."""
+    q4 = lib()
+    g = synth.generator(8300)
+    N, K = 300, 2048
+    w = synth.weights(g, N, K) * np.float32(0.03)                  # |d| around 2^-12
+    blocks = w.reshape(N, K // 32, 32)
+    sub = g.random((N, K // 32)) < 0.2
+    blocks[sub] *= np.float32(1e-3)                                # subnormal binary16 scales
+    blocks[g.random((N, K // 32)) < 0.05] = 0.0                    # d = +0
+    wq = oracle.get().quantize(w)
+    codes, dbits = oracle.get().unpack(wq, N, K)
+    assert ((dbits & 0x7C00) < 0x1400).all()
+    assert ((dbits & 0x7C00) == 0).any() and ((dbits & 0x7FFF) != 0).any() and (dbits == 0).any()
+    for M in (4, 20, 64):
+        x = synth.to_bf16_bits(synth.activations_f32(g, M, K))
+        check_full(q4.matmul(x_dev(x), wq_dev(wq), N, K), x, wq, N, K)
+
+
 def test_gemv_and_gemm_agree():
     q4 = lib()
     for M in (1, 16, 32):
