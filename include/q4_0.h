@@ -100,17 +100,17 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
  * |y - y_exact| <= 1e-2 * sum_k |w x| and relative L2 error <= 2e-3.
  * Activations must be finite with |x| <= 65504 (the tensor-core paths round
  * x to binary16).
- * Scratch: the GEMM path needs q4_0_matmul_workspace_bytes(M, N, K) bytes;
- * this entry point takes them with cudaMallocAsync on `stream` and frees
- * them with cudaFreeAsync on the same stream.  Use q4_0_matmul_ws to supply
- * the workspace yourself.
+ * Scratch: the batched-decode (3 <= M <= 32) and GEMM (M > 32) paths need
+ * q4_0_matmul_workspace_bytes(M, N, K) bytes; this entry point takes them
+ * with cudaMallocAsync on `stream` and frees them with cudaFreeAsync on the
+ * same stream.  Use q4_0_matmul_ws to supply the workspace yourself.
  * Alignment: x, wq and y 16 bytes.
  * Returns Q4_0_OK, Q4_0_ERR_INVALID_ARG, Q4_0_ERR_UNSUPPORTED or Q4_0_ERR_CUDA.
  */
 int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y,
                 int64_t M, int64_t N, int64_t K, void *stream);
 
-/* Scratch bytes q4_0_matmul needs for these sizes (0 for the GEMV path). */
+/* Scratch bytes q4_0_matmul needs for these sizes (0 for M <= 2). */
 size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -128,12 +128,29 @@ int q4_0_matmul_ws(const uint16_t *x, const uint8_t *wq, float *y,
                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * q4_0_gemv -- the decode kernel alone (what q4_0_matmul runs for M <= 32).
- * Same arguments, layout and result contract as q4_0_matmul; M <= 32
- * (larger M is UNSUPPORTED).  Needs no workspace.
+ * q4_0_gemv -- the decode kernels alone (what q4_0_matmul runs for
+ * M <= 32).  Same arguments, layout and result contract as q4_0_matmul;
+ * M <= 32 (larger M is UNSUPPORTED).  M <= 2 needs no scratch; for
+ * 3 <= M <= 32 x is first rounded to binary16 tensor-core tiles in
+ * q4_0_gemv_workspace_bytes(M, K) bytes of scratch, which this entry point
+ * takes with cudaMallocAsync / cudaFreeAsync on `stream`.
  */
 int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y,
               int64_t M, int64_t N, int64_t K, void *stream);
+
+/* Scratch bytes of the decode kernels (0 for M <= 2 or M > 32). */
+size_t q4_0_gemv_workspace_bytes(int64_t M, int64_t K);
+
+/*
+ * q4_0_gemv_ws -- q4_0_gemv with caller-owned scratch: workspace 256-byte
+ * aligned, at least q4_0_gemv_workspace_bytes(M, K) bytes (may be NULL when
+ * that is 0), in use until the work on `stream` completes.  Returns
+ * Q4_0_ERR_WORKSPACE when it is missing, misaligned or too small, otherwise
+ * as q4_0_gemv.
+ */
+int q4_0_gemv_ws(const uint16_t *x, const uint8_t *wq, float *y,
+                 int64_t M, int64_t N, int64_t K,
+                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * q4_0_gemm -- the tcgen05 prefill kernel alone (what q4_0_matmul runs for

@@ -33,6 +33,8 @@ SIGNATURES = {
     "q4_0_matmul_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "q4_0_matmul_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemv": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "q4_0_gemv_workspace_bytes": ([_I64, _I64], _SZ),
+    "q4_0_gemv_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemm_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "q4_0_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemm_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
@@ -165,8 +167,19 @@ def matmul_alloc(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.T
 
 
 def gemv(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
-         stream=None) -> torch.Tensor:
-    """The decode kernel alone (M <= 32)."""
+         workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """The decode kernels alone (M <= 32), through q4_0_gemv_ws."""
+    M, out = _mm_args(x, wq, N, K, out)
+    ws, wsb = _workspace(int(lib().q4_0_gemv_workspace_bytes(M, K)), x.device, workspace)
+    _check(lib().q4_0_gemv_ws(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
+                              ws.data_ptr() if ws is not None else None, wsb, _stream(stream)),
+           "q4_0_gemv")
+    return out
+
+
+def gemv_alloc(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
+               stream=None) -> torch.Tensor:
+    """Same as gemv, through q4_0_gemv (the library takes its own scratch)."""
     M, out = _mm_args(x, wq, N, K, out)
     _check(lib().q4_0_gemv(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)),
            "q4_0_gemv")

@@ -157,9 +157,28 @@ size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return gemm_workspace_bytes(M, N, K, current_splits(M, N, K));
 }
 
+size_t q4_0_gemv_workspace_bytes(int64_t M, int64_t K) {
+    if (M < 1 || M > 32 || K < 1) return 0;
+    return gemv_workspace_bytes(M, K);
+}
+
 size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    if (M <= 32) return 0;
+    if (M <= 32) return q4_0_gemv_workspace_bytes(M, K);
     return q4_0_gemm_workspace_bytes(M, N, K);
+}
+
+int q4_0_gemv_ws(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+                 void *workspace, size_t workspace_bytes, void *stream) {
+    int st = check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    if (M > 32) return Q4_0_ERR_UNSUPPORTED;
+    const size_t need = gemv_workspace_bytes(M, K);
+    if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return Q4_0_ERR_WORKSPACE;
+    unsigned int *err = device_error_word();
+    if (!err) return Q4_0_ERR_CUDA;
+    return from_cuda(launch_gemv(x, wq, y, M, N, K, need ? workspace : nullptr,
+                                 static_cast<cudaStream_t>(stream), err));
 }
 
 int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
@@ -167,9 +186,15 @@ int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
     if (M > 32) return Q4_0_ERR_UNSUPPORTED;
-    unsigned int *err = device_error_word();
-    if (!err) return Q4_0_ERR_CUDA;
-    return from_cuda(launch_gemv(x, wq, y, M, N, K, static_cast<cudaStream_t>(stream), err));
+    const size_t bytes = gemv_workspace_bytes(M, K);
+    if (bytes == 0) return q4_0_gemv_ws(x, wq, y, M, N, K, nullptr, 0, stream);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return Q4_0_ERR_CUDA;
+    st = q4_0_gemv_ws(x, wq, y, M, N, K, ws, bytes, stream);
+    const cudaError_t fe = cudaFreeAsync(ws, s);
+    if (st == Q4_0_OK && fe != cudaSuccess) st = Q4_0_ERR_CUDA;
+    return st;
 }
 
 int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
@@ -192,7 +217,7 @@ int q4_0_matmul_ws(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, in
                    void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
-    if (M <= 32) return q4_0_gemv(x, wq, y, M, N, K, stream);
+    if (M <= 32) return q4_0_gemv_ws(x, wq, y, M, N, K, workspace, workspace_bytes, stream);
     return q4_0_gemm(x, wq, y, M, N, K, workspace, workspace_bytes, stream);
 }
 

@@ -654,8 +654,12 @@ cudaError_t launch(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, in
 
 }  // namespace
 
+size_t gemv_workspace_bytes(int64_t M, int64_t K) {
+    return M >= 3 && M <= 32 ? gemv_tc_workspace_bytes(M, K) : 0;
+}
+
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
-                        int64_t K, cudaStream_t s, unsigned int *err) {
+                        int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -670,7 +674,7 @@ cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t 
         if (e != cudaSuccess || done) return e;
     } else {
         // three or more rows of x: the dot product moves to the tensor cores
-        return launch_gemv_tc(x, wq, y, M, N, K, s, err);
+        return launch_gemv_tc(x, wq, y, M, N, K, workspace, s, err);
     }
     // rows of x per launch: the largest power of two <= 8 that covers M (or
     // fits shared memory); each launch streams the weights once

@@ -12,10 +12,12 @@
 //     one MMA-warp iteration issues the slot's eight MMAs (the issuing warp
 //     shares its scheduler with the dequant warps, so fewer, larger
 //     iterations keep it off the critical path);
-//   * B = x: two warps load bf16 x with plain 16-byte loads (x is small and
-//     L2-resident; tensor copies of it would queue behind the weight stream),
-//     round to binary16 and write the 128-byte-swizzled K-major layout the
-//     MMA reads -- no scratch buffer;
+//   * B = x: a small kernel first rounds x to binary16 once per call, already
+//     in the 128-byte-swizzled K-major tiles the MMA reads (rows >= M zero),
+//     into a workspace of TM * K * 2 bytes; every CTA then brings in each
+//     stage's x tile with one bulk copy.  Converting inside every CTA would
+//     repeat the same work once per weight tile and load the schedulers of
+//     two SM quarters more than the others;
 //   * D = 128 x TM fp32 in tensor memory (TM = 16 or 32, padded rows of x are
 //     zero);
 //   * N is tiled by 128 rows; K is split over the CTAs of a thread-block
@@ -41,10 +43,9 @@ constexpr int kKW = 256;                  // k per weight stage
 constexpr int kSubs = kKW / kKB;          // A slots per weight stage
 constexpr int kWRowBytes = kKW / 32 * 18;  // 144
 constexpr int kWStageBytes = kTileN * kWRowBytes;
-constexpr int kNW = 3, kNX = 2, kNA = 3;  // 32 + 3 x 64 TMEM columns <= 256
+constexpr int kNW = 3, kNA = 3;  // 32 + 3 x 64 TMEM columns <= 256
 constexpr int kDequantWarps = 8;
-constexpr int kConvertWarps = 2;
-constexpr int kThreads = 32 * (2 + kDequantWarps + kConvertWarps);  // 384
+constexpr int kThreads = 32 * (2 + kDequantWarps);  // 320
 constexpr int kMaxCluster = 8;
 
 __host__ __device__ constexpr uint32_t cols_pow2(uint32_t v) {
@@ -57,6 +58,7 @@ template <int TM>
 struct Cfg {
     static constexpr uint32_t kXAtom = TM * 128;             // [TM x 64 k] fp16, 128-byte swizzle
     static constexpr uint32_t kXStage = kXAtom * (kKW / 64);   // one weight stage of k
+    static constexpr int kNX = TM <= 16 ? 4 : 2;                // x ring (two CTAs fit an SM)
     static constexpr uint32_t kDCols = 32;
     static constexpr uint32_t kCols = cols_pow2(kDCols + kNA * (kKB / 2));
     static constexpr int kPartStride = TM + 1;  // floats per row of the partial tile
@@ -116,11 +118,42 @@ __device__ __forceinline__ void swap_mid_pairs(uint32_t &a, uint32_t &b) {
     b = hi;
 }
 
+// x (bf16, [M][K]) -> the binary16 B tiles of gemv_tc_kernel: stage u (256 k)
+// is four atoms [TM rows x 64 k]; in an atom, row m is 128 bytes whose
+// 16-byte chunk c sits at position c ^ (m & 7) (the 128-byte swizzle named in
+// the MMA's shared-memory descriptor), values in the k order of the weight
+// tiles; rows m >= M are zero.  One thread per 16-byte chunk.
+template <int TM>
+__global__ void __launch_bounds__(256) x_tiles_kernel(const uint16_t *__restrict__ x, uint4 *__restrict__ xt,
+                                                      int M, int K) {
+    pdl_launch_dependents();
+    pdl_wait();  // x may come from the previous kernel
+    const int kc8 = K / 8;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)TM * kc8) return;
+    const int m = (int)(i / kc8), kc = (int)(i - (int64_t)m * kc8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (m < M) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)m * K) + kc);
+        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            o[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16), __uint_as_float(in[h] & 0xFFFF0000u)));
+        swap_mid_pairs(o[0], o[1]);
+        swap_mid_pairs(o[2], o[3]);
+        v = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    const int u = kc >> 5, a = (kc >> 3) & 3, c = kc & 7;
+    xt[((int64_t)(u * 4 + a) * TM + m) * 8 + (c ^ (m & 7))] = v;
+}
+
 template <int TM>
 __global__ void __launch_bounds__(kThreads, 2)
-    gemv_tc_kernel(const uint16_t *__restrict__ x, const __grid_constant__ CUtensorMap wmap,
+    gemv_tc_kernel(const uint4 *__restrict__ xt, const __grid_constant__ CUtensorMap wmap,
                    float *__restrict__ y, int M, int N, int K, unsigned int *err) {
     using C = Cfg<TM>;
+    constexpr int kNX = C::kNX;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -129,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *part = reinterpret_cast<float *>(smem + C::kOffPart);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);
     uint64_t *w_full = bars, *w_empty = bars + kNW;
-    uint64_t *x_conv = bars + 2 * kNW, *x_empty = x_conv + kNX;
+    uint64_t *x_full = bars + 2 * kNW, *x_empty = x_full + kNX;
     uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNA;
     uint64_t *d_full = a_empty + kNA, *drain = d_full + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
@@ -149,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(&w_empty[i], kDequantWarps);  // one arrival per warp
         }
         for (int i = 0; i < kNX; ++i) {
-            mbar_init(&x_conv[i], kConvertWarps);
+            mbar_init(&x_full[i], 1);
             mbar_init(&x_empty[i], 1);
         }
         for (int i = 0; i < kNA; ++i) {
@@ -172,37 +205,57 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == 0) {
         if (lane == 0) {
-            // weight stream (weights may be fetched before the previous kernel
-            // ends; x is fetched by the converter warps after pdl_wait)
+            // copies: the first weight stages go out before the wait for the
+            // previous kernel (weights do not depend on it); then, per stage,
+            // its x tile and the weight stage kNW ahead
             const uint64_t policy = l2_evict_first_policy();  // weights are read once
-            int issued_w = 0;
-            for (int ws = 0; ws < nW; ++ws) {
+            int issued_w = 0, issued_x = 0;
+            auto issue_w = [&](int ws) -> bool {
                 const int wsl = ws % kNW;
-                if (!mbar_wait(&w_empty[wsl], ((ws / kNW) & 1) ^ 1, abort_flag, err)) break;
+                if (!mbar_wait(&w_empty[wsl], ((ws / kNW) & 1) ^ 1, abort_flag, err)) return false;
                 mbar_arrive_expect_tx(&w_full[wsl], kWStageBytes);
                 tma_load_2d_hint(wring + wsl * kWStageBytes, &wmap, (u0 + ws) * kWRowBytes, n0, &w_full[wsl],
                                  policy);
                 ++issued_w;
+                return true;
+            };
+            auto issue_x = [&](int ws) -> bool {
+                const int xsl = ws % kNX;
+                if (!mbar_wait(&x_empty[xsl], ((ws / kNX) & 1) ^ 1, abort_flag, err)) return false;
+                mbar_arrive_expect_tx(&x_full[xsl], C::kXStage);
+                bulk_g2s(xring + xsl * C::kXStage, xt + (size_t)(u0 + ws) * (C::kXStage / 16), C::kXStage,
+                         &x_full[xsl]);
+                ++issued_x;
+                return true;
+            };
+            bool ok = true;
+            for (int ws = 0; ok && ws < kNW && ws < nW; ++ws) ok = issue_w(ws);
+            pdl_wait();  // the x tiles come from the previous kernel
+            for (int ws = 0; ok && ws < nW; ++ws) {
+                ok = issue_x(ws);
+                if (ok && ws + kNW < nW) ok = issue_w(ws + kNW);
             }
+            // let every issued copy land before the CTA can exit
             for (int i = issued_w - kNW; i < issued_w; ++i)
                 if (i >= 0) mbar_drain(&w_full[i % kNW], (i / kNW) & 1);
+            for (int i = issued_x - kNX; i < issued_x; ++i)
+                if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
         }
     } else if (warp == 1) {
         // MMA issue: the whole warp waits and loops (converged); one elected
         // lane issues the MMAs and commits
         constexpr uint32_t idesc = idesc_f16_f32(kTileN, TM);
-        for (int s = 0; s < nS; ++s) {
-            const int ws = s / kSubs, sub = s % kSubs;
-            const int xsl = ws % kNX, asl = s % kNA;
-            if (sub == 0 &&
-                !__all_sync(0xffffffffu, mbar_wait(&x_conv[xsl], (ws / kNX) & 1, abort_flag, err)))
-                break;
-            if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err))) break;
+        const uint64_t bdesc0 = smem_desc_k128(xring);
+        // one A slot: wait for its x tile (first slot of a stage) and its
+        // dequantised weights, issue its eight MMAs, release both.  x atoms of
+        // 64 k are contiguous, so the descriptor's start address moves by one
+        // atom every four MMAs.
+        auto slot = [&](int s, int sub, int xsl, int asl, uint32_t xpar, uint32_t apar) -> bool {
+            if (sub == 0 && !__all_sync(0xffffffffu, mbar_wait(&x_full[xsl], xpar, abort_flag, err))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], apar, abort_flag, err))) return false;
             tc_fence_after();
             if (elect_one()) {
-                // x atoms of 64 k are contiguous: the descriptor's start address
-                // moves by one atom every four MMAs
-                const uint64_t bdesc = smem_desc_k128(xring + xsl * C::kXStage + sub * (kKB / 64) * C::kXAtom);
+                const uint64_t bdesc = bdesc0 + ((xsl * C::kXStage + sub * (kKB / 64) * C::kXAtom) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk)
                     mma_f16_ts(d_tmem, a_tmem + asl * (kKB / 2) + kk * 8,
@@ -211,6 +264,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (sub == kSubs - 1) mma_commit(&x_empty[xsl]);
             }
             __syncwarp();
+            return true;
+        };
+        bool ok = true;
+        for (int s = 0; ok && s < nS; ++s) {
+            const int ws = s / kSubs;
+            ok = slot(s, s % kSubs, ws % kNX, s % kNA, (uint32_t)(ws / kNX) & 1u, (uint32_t)(s / kNA) & 1u);
         }
         if (elect_one()) mma_commit(d_full);
         __syncwarp();
@@ -285,47 +344,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
-    } else {
-        // x converters: per weight stage, load x[0:M][k0:k0+256] (bf16, 16 bytes
-        // per load), round to binary16 and store into the four 64-k atoms in
-        // the 128-byte-swizzled layout (16-byte chunk c of row m lands at
-        // chunk c ^ (m & 7)); rows m >= M are zero
-        const int t = threadIdx.x - 32 * (2 + kDequantWarps);
-        constexpr int kChunks = TM * (kKW / 8);                 // 16-byte chunks per stage
-        constexpr int kPer = kChunks / (32 * kConvertWarps);    // per thread
-        pdl_wait();  // x may come from the previous kernel
-        for (int ws = 0; ws < nW; ++ws) {
-            const int xsl = ws % kNX;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xsl], ((ws / kNX) & 1) ^ 1, abort_flag, err));
-            if (!ok) break;
-            const int64_t k0 = (int64_t)(u0 + ws) * kKW;
-            uint4 v[kPer];
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                const int i = t + j * 32 * kConvertWarps, m = i / (kKW / 8), c = i % (kKW / 8);
-                v[j] = m < M ? __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)m * K + k0) + c)
-                             : make_uint4(0, 0, 0, 0);
-            }
-            uint8_t *stage = xring + xsl * C::kXStage;
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                const int i = t + j * 32 * kConvertWarps, m = i / (kKW / 8), c = i % (kKW / 8);
-                const uint32_t in[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                uint32_t o[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h)
-                    o[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16),
-                                                 __uint_as_float(in[h] & 0xFFFF0000u)));
-                swap_mid_pairs(o[0], o[1]);  // the k order of the weight tiles
-                swap_mid_pairs(o[2], o[3]);
-                const int atom = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4 *>(stage + atom * C::kXAtom + m * 128 + ((cc ^ (m & 7)) << 4)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&x_conv[xsl]);
-        }
     }
 
     // cluster reduction: CTA `rank` sums rows [rank * rpc, ...) of the S
@@ -384,7 +402,7 @@ EncodeTiledFn encode_fn() {
 
 template <int TM>
 cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
-                      cudaStream_t s, unsigned int *err) {
+                      void *xtiles, cudaStream_t s, unsigned int *err) {
     using C = Cfg<TM>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -413,16 +431,26 @@ cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M,
     S = S < 1 ? 1 : (S > kMaxCluster ? kMaxCluster : S);
     if (S > KU) S = KU;
     if (tiles > 65535) return cudaErrorInvalidValue;
+    const int64_t chunks = (int64_t)TM * (K / 8);
+    e = launch_pdl(x_tiles_kernel<TM>, dim3((unsigned)((chunks + 255) / 256)), dim3(256), 0, s, x,
+                   static_cast<uint4 *>(xtiles), (int)M, (int)K);
+    if (e != cudaSuccess) return e;
     return launch_pdl_cluster(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads),
-                              C::kSmem, s, (unsigned)S, x, wmap, y, (int)M, (int)N, (int)K, err);
+                              C::kSmem, s, (unsigned)S, static_cast<const uint4 *>(xtiles), wmap, y, (int)M,
+                              (int)N, (int)K, err);
 }
 
 }  // namespace
 
+size_t gemv_tc_workspace_bytes(int64_t M, int64_t K) {
+    const int64_t tm = M <= 16 ? 16 : 32;
+    return (size_t)(tm * K * 2);
+}
+
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
-                           int64_t K, cudaStream_t s, unsigned int *err) {
-    if (M <= 16) return launch_tm<16>(x, wq, y, M, N, K, s, err);
-    return launch_tm<32>(x, wq, y, M, N, K, s, err);
+                           int64_t K, void *xtiles, cudaStream_t s, unsigned int *err) {
+    if (M <= 16) return launch_tm<16>(x, wq, y, M, N, K, xtiles, s, err);
+    return launch_tm<32>(x, wq, y, M, N, K, xtiles, s, err);
 }
 
 }  // namespace q4_0

@@ -60,13 +60,18 @@ cudaError_t launch_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, c
                             unsigned int *err);
 
 // Decode GEMV for M <= 32 (x, y point at row 0; row strides K and N).
+// `workspace` (256-byte aligned, gemv_workspace_bytes(M, K) bytes) is used for
+// 3 <= M <= 32 only.
+size_t gemv_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
-                        int64_t K, cudaStream_t s, unsigned int *err);
+                        int64_t K, void *workspace, cudaStream_t s, unsigned int *err);
 
-// Tensor-core decode for 3 <= M <= 32: split-K over a thread-block cluster,
-// no scratch memory.
+// Tensor-core decode for 3 <= M <= 32: x rounded once into binary16 MMA
+// tiles in `xtiles` (gemv_tc_workspace_bytes(M, K) bytes), then split-K over
+// a thread-block cluster.
+size_t gemv_tc_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
-                           int64_t K, cudaStream_t s, unsigned int *err);
+                           int64_t K, void *xtiles, cudaStream_t s, unsigned int *err);
 
 // tcgen05 GEMM.  `workspace` holds x rounded to binary16 and, when K is
 // split (splits > 1), the fp32 partial tiles: gemm_workspace_bytes(M, N, K,

@@ -54,7 +54,15 @@ def test_weight_bytes(lib):
 
 def test_workspace_sizes(lib):
     assert lib.q4_0_matmul_workspace_bytes(1, 5120, 5120) == 0
-    assert lib.q4_0_matmul_workspace_bytes(32, 5120, 5120) == 0
+    assert lib.q4_0_matmul_workspace_bytes(2, 5120, 5120) == 0
+    # batched decode: x as binary16 tiles of 16 or 32 rows
+    assert lib.q4_0_matmul_workspace_bytes(3, 5120, 5120) == 16 * 5120 * 2
+    assert lib.q4_0_matmul_workspace_bytes(16, 5120, 17408) == 16 * 17408 * 2
+    assert lib.q4_0_matmul_workspace_bytes(17, 5120, 5120) == 32 * 5120 * 2
+    assert lib.q4_0_matmul_workspace_bytes(32, 5120, 5120) == 32 * 5120 * 2
+    for M in (1, 2, 3, 16, 17, 32):
+        assert lib.q4_0_gemv_workspace_bytes(M, 5120) == lib.q4_0_matmul_workspace_bytes(M, 7, 5120)
+    assert lib.q4_0_gemv_workspace_bytes(33, 5120) == 0
     assert lib.q4_0_matmul_workspace_bytes(33, 5120, 5120) == 33 * 5120 * 2
     assert lib.q4_0_gemm_workspace_bytes(3, 128, 256) % 256 == 0
 
@@ -69,6 +77,9 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.q4_0_matmul(good, good, good, 1, 1, 96, None) == -2     # K % 256
     assert lib.q4_0_matmul(P((1 << 20) + 8), good, good, 1, 1, 256, None) == -1  # misaligned
     assert lib.q4_0_gemv(good, good, good, 33, 1, 256, None) == -2
+    assert lib.q4_0_gemv_ws(good, good, good, 16, 1, 256, None, 0, None) == -5
+    assert lib.q4_0_gemv_ws(good, good, good, 16, 1, 256, P((1 << 20) + 16), 1 << 20, None) == -5
+    assert lib.q4_0_gemv_ws(good, good, good, 16, 1, 256, good, 16 * 256 * 2 - 1, None) == -5
     assert lib.q4_0_gemm(good, good, good, 64, 1, 256, None, 0, None) == -5
     assert lib.q4_0_gemm(good, good, good, 64, 1, 256, P((1 << 20) + 16), 1 << 20, None) == -5
     assert lib.q4_0_quantize(None, good, 1, 32, None) == -1

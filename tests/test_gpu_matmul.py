@@ -169,6 +169,29 @@ def test_device_argument_errors():
     assert q4.device_error() == 0
 
 
+def test_gemv_scratch_paths_agree():
+    """q4_0_gemv (library-allocated scratch) and q4_0_gemv_ws (caller's
+    workspace, here with slack) give identical bits; a workspace one byte
+    short is refused before anything is launched."""
+    q4 = lib()
+    for M in (1, 3, 16, 17, 32):
+        x, wq = case(7100 + M, M, 300, 1536)
+        xd, wd = x_dev(x), wq_dev(wq)
+        a = q4.gemv(xd, wd, 300, 1536)
+        need = q4.lib().q4_0_gemv_workspace_bytes(M, 1536)
+        ws = torch.empty(need + 4096, dtype=torch.uint8, device="cuda")
+        b = q4.gemv(xd, wd, 300, 1536, workspace=ws)
+        c = q4.gemv_alloc(xd, wd, 300, 1536)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b) and torch.equal(a, c)
+        if need:
+            y = torch.empty((M, 300), dtype=torch.float32, device="cuda")
+            st = q4.lib().q4_0_gemv_ws(xd.data_ptr(), wd.data_ptr(), y.data_ptr(), M, 300, 1536,
+                                       ws.data_ptr(), need - 1, None)
+            assert st == q4.ERR_WORKSPACE
+    assert q4.device_error() == 0
+
+
 # --------------------------------------------------------- workload sizes
 
 def test_pr1():
