@@ -243,7 +243,8 @@ def run_ours(args, rank, world, local):
         with torch.cuda.graph(full, stream=stream):
             for v in range(cycle):
                 enqueue_step(v)
-    launches_per_step = 4 * (layers if sweep else 1)
+    calls_per_step = len(shapes) * (layers if sweep else 1)
+    launches_per_step = sum(kernels_per_call(q4, M, N, K) for _, (N, K) in shapes) * (layers if sweep else 1)
 
     def run_steps(n):
         for _ in range(n // cycle):
@@ -309,18 +310,19 @@ def run_ours(args, rank, world, local):
     value = gbs if M < 256 else tflops
     # roofline of the dominant kernel (the only kernel in the timed region)
     launches = args.steps * launches_per_step
+    calls = args.steps * calls_per_step  # launches of the dominant kernel (one per matmul)
     if M < 256:
         roof = {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(gbs / world / hbm, 4), "traffic": None,
-                "kernel": "gemv_dp4a_kernel<1>" if M == 1 else ("gemv_dp4a_kernel<2>" if M == 2 else "gemv_kernel"),
-                "peak_source": peak_kind, "bytes_per_launch": round(step_bytes / launches_per_step),
-                "avg_launch_us": round(ms_local * 1e3 / launches, 3)}
+                "kernel": dominant_kernel(M), "peak_source": peak_kind,
+                "bytes_per_launch": round(step_bytes / calls_per_step),
+                "avg_launch_us": round(ms_local * 1e3 / calls, 3)}
     else:
         roof = {"bound": "tensor", "achieved": round(tflops / world, 1), "peak": tf_sust,
                 "unit": "TFLOP/s", "frac": round(tflops / world / tf_sust, 4), "traffic": None,
-                "kernel": "gemm_kernel<256>", "peak_source": peak_kind + " sustained",
-                "avg_launch_us": round(ms_local * 1e3 / launches, 3)}
-    traffic = load_traffic(args.workload)
+                "kernel": dominant_kernel(M), "peak_source": peak_kind + " sustained",
+                "avg_launch_us": round(ms_local * 1e3 / calls, 3)}
+    traffic = load_traffic(args.workload, M)
     if traffic is not None:
         roof["traffic"] = traffic
 
@@ -328,8 +330,8 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": warm, "ms_per_step": round(ms / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "q4_0 weights; f16 FMA in-block, f32 across blocks" if M < 256 else
-                 "q4_0 weights -> f16 tiles; f16 MMA, f32 accumulate",
+        "dtype": ("q4_0 codes x 15-bit fixed-point x: int dp4a in-block, f32 across blocks" if M <= 2 else
+                  "q4_0 weights -> f16 tiles; f16 MMA, f32 accumulate"),
         "data": "synthetic: W ~ N(0, 0.02) quantized on device, x ~ N(0, 1) bf16",
         "config": {"workload": workload_name(args.workload, M, layers), "M": M,
                    "shapes": {s: list(nk) for s, nk in shapes}, "layer_copies": layers,
@@ -359,10 +361,30 @@ def workload_name(w, M, layers):
                        f"four matrices per step, {layers} layer copies"}[w]
 
 
-def load_traffic(workload):
+def kernels_per_call(q4, M, N, K):
+    """Kernels one q4_0_matmul call launches: the integer-dot decode
+    (M <= 2); x tiles + tensor-core decode (3 <= M <= 32); x -> binary16 +
+    GEMM, plus the split-K sum when the workspace holds partial tiles."""
+    if M <= 2:
+        return 1
+    if M <= 32:
+        return 2
+    x16 = (M * K * 2 + 255) // 256 * 256
+    return 3 if q4.lib().q4_0_gemm_workspace_bytes(M, N, K) > x16 else 2
+
+
+def dominant_kernel(M):
+    if M <= 2:
+        return f"gemv_dp4a_kernel<{M}>"
+    if M <= 32:
+        return f"gemv_tc_kernel<{16 if M <= 16 else 32}>"
+    return "gemm_kernel"
+
+
+def load_traffic(workload, M):
     """DRAM bytes per launch of the dominant kernel, from the committed ncu
     summary (profiles/traffic.json); None when there is none for this
-    workload or the kernel source has changed since it was captured."""
+    workload and M or the kernel source has changed since it was captured."""
     import hashlib
     path = os.path.join(HERE, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -370,7 +392,7 @@ def load_traffic(workload):
     try:
         with open(path) as f:
             d = json.load(f).get(workload)
-        if not d:
+        if not d or d.get("M") != M:
             return None
         with open(os.path.join(HERE, d["kernel_source"]), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest()[:16] != d["sha256_16"]:
