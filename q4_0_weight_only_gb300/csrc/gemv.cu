@@ -439,6 +439,7 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bars);
     uint64_t *empty = full + a.S;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + a.S);
+    uint64_t *xready = empty + a.S + 1;  // x converted (the compute threads' signal to the producer)
     float *part = reinterpret_cast<float *>(smem + a.off_part);  // [rows][H][MT]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -468,6 +469,7 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], nwc);
         }
+        mbar_init(xready, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -478,9 +480,19 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
 
     if (warp == nwc) {
         // Weights are read before pdl_wait(): no kernel of this library
-        // writes Q4_0 weights while a dependent matmul may be running.
+        // writes Q4_0 weights while a dependent matmul may be running.  The
+        // first stages go out at once; the rest of the ring waits until x is
+        // converted: a CTA that starts after the previous kernel has ended
+        // would otherwise find its x loads queued behind a ring's worth of
+        // weight bytes arriving at the same SM, and such a late CTA decides
+        // when the kernel ends.
         if (lane == 0) {
-            for (int i = 0; i < a.S && i < nst; ++i) issue(i);
+            constexpr int kPreWait = 3;
+            const int pre = min(kPreWait, min(a.S, nst));
+            for (int i = 0; i < pre; ++i) issue(i);
+            pdl_wait();
+            mbar_wait(xready, 0, abort_flag, err);
+            for (int i = pre; i < a.S && i < nst; ++i) issue(i);
             int issued = min(a.S, nst);
             for (int i = a.S; i < nst; ++i) {
                 if (!mbar_wait(&empty[i % a.S], ((i / a.S) & 1) ^ 1, abort_flag, err)) break;
@@ -507,6 +519,7 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
                      xsm + ((size_t)m * a.P + (b >> 1)) * kPairWords);
     }
     asm volatile("bar.sync 1, %0;" ::"r"(a.T) : "memory");
+    if (tid == 0) mbar_arrive(xready);
 
     const int pc = tid % a.P, rs = tid / a.P;
     const bool active = rs < a.c;
@@ -623,7 +636,7 @@ Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
     a.off_x = (uint32_t)off;
     off += (size_t)mt * a.P * kPairWords * 4;
     a.off_bars = (uint32_t)off;
-    off += (size_t)2 * a.S * 8 + 16;
+    off += (size_t)2 * a.S * 8 + 16;  // full[S], empty[S], then the abort flag and the x-ready barrier
     a.off_part = (uint32_t)off;
     off += (size_t)rows_cap * a.H * mt * 4;
     p.smem = off;
