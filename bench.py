@@ -36,8 +36,8 @@ LAYER_WEIGHTS_64 = 21.139e9  # Q4_0 weights in 64 layers of the four matrices
 METRIC = "Q4_0 matmul: decode GB/s (% HBM peak), prefill TFLOP/s, tok/s-equivalent"
 
 
-def alg_bytes(M, N, K):
-    return 0.5625 * N * K + 2 * M * K + 4 * M * N
+def alg_bytes(M, N, K, y_bytes=4):
+    return 0.5625 * N * K + 2 * M * K + y_bytes * M * N
 
 
 def parse():
@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--layers", type=int, default=8, help="resident layer copies (decode/batched)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--y-dtype", choices=["f32", "bf16"], default="f32",
+                   help="element type of y (bf16: the rounded-once output of q4_0_matmul_ex)")
     return p.parse_args()
 
 
@@ -208,14 +210,16 @@ def run_ours(args, rank, world, local):
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     xs = [torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16) for _, (N, K) in shapes]
-    ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _, (N, K) in shapes]
+    ydt = torch.bfloat16 if args.y_dtype == "bf16" else torch.float32
+    ysz = 2 if args.y_dtype == "bf16" else 4
+    ys = [torch.empty((M, N), dtype=ydt, device=dev) for _, (N, K) in shapes]
     wss = [torch.empty(max(1, q4.lib().q4_0_matmul_workspace_bytes(M, N, K)), dtype=torch.uint8,
                        device=dev) for _, (N, K) in shapes]
     stream = torch.cuda.Stream(device=dev)
 
     sweep = args.workload == "sweep"
     per_step_layers = layers if sweep else 1  # a sweep step passes through every layer
-    step_bytes = per_step_layers * sum(alg_bytes(M, N, K) for _, (N, K) in shapes)
+    step_bytes = per_step_layers * sum(alg_bytes(M, N, K, ysz) for _, (N, K) in shapes)
     step_flops = per_step_layers * sum(2.0 * M * N * K for _, (N, K) in shapes)
     step_weights = per_step_layers * sum(N * K for _, (N, K) in shapes)
 
@@ -223,7 +227,7 @@ def run_ours(args, rank, world, local):
         ls = range(layers) if sweep else (i % layers,)
         for l in ls:
             for j, (_, (N, K)) in enumerate(shapes):
-                q4.matmul(xs[j], wq[l][j], N, K, out=ys[j], workspace=wss[j], stream=stream)
+                q4.matmul(xs[j], wq[l][j], N, K, out=ys[j], workspace=wss[j], stream=stream, out_dtype=ydt)
 
     # CUDA graphs: one graph per full cycle of the resident layer copies (a
     # decode engine captures a whole pass the same way), plus one graph per
@@ -287,9 +291,9 @@ def run_ours(args, rank, world, local):
     x_host = [torch.empty((M, K), dtype=torch.bfloat16).pin_memory() for _, (N, K) in shapes]
     for j, xh in enumerate(x_host):
         xh.copy_(xs[j].cpu())
-    y_host = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _, (N, K) in shapes]
+    y_host = [torch.empty((M, N), dtype=ydt).pin_memory() for _, (N, K) in shapes]
     h2d = sum(x.numel() * 2 for x in x_host) * (layers if sweep else 1)
-    d2h = sum(y.numel() * 4 for y in y_host) * (layers if sweep else 1)
+    d2h = sum(y.numel() * ysz for y in y_host) * (layers if sweep else 1)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
@@ -299,7 +303,8 @@ def run_ours(args, rank, world, local):
             for l in ls:
                 for j, (_, (N, K)) in enumerate(shapes):
                     xs[j].copy_(x_host[j], non_blocking=True)
-                    q4.matmul(xs[j], wq[l][j], N, K, out=ys[j], workspace=wss[j], stream=stream)
+                    q4.matmul(xs[j], wq[l][j], N, K, out=ys[j], workspace=wss[j], stream=stream,
+                              out_dtype=ydt)
                     y_host[j].copy_(ys[j], non_blocking=True)
             stream.synchronize()
     t_e2e = max_over_ranks(time.perf_counter() - t0, world)
@@ -337,7 +342,7 @@ def run_ours(args, rank, world, local):
                    "shapes": {s: list(nk) for s, nk in shapes}, "layer_copies": layers,
                    "l2": "inputs larger than L2: %d resident layer copies, %.2f GB cycled"
                          % (layers, layers * sum(0.5625 * N * K for _, (N, K) in shapes) / 1e9),
-                   "parallelism": f"replicas x{world}",
+                   "y": args.y_dtype, "parallelism": f"replicas x{world}",
                    "graph": f"one CUDA graph per {cycle} step(s), replayed; PDL between kernels"},
         "tok_s_eq": round(tok_s, 1),
         "tflops": round(tflops, 2),
@@ -430,6 +435,7 @@ def cpu_baseline(wq_layer, xs, shapes, M, budget_s=10.0):
 def run_reference(args, rank, world, local):
     """The oracle as the reference arm: each step is a bounded sample of the
     workload (a slice of rows of each matrix) on the host cores."""
+    ref_layers = 64 if args.workload == "sweep" else (1 if args.workload == "prefill" else args.layers)
     if rank != 0:
         return None
     import oracle
@@ -460,7 +466,7 @@ def run_reference(args, rank, world, local):
         for N, K, wq, x in host:
             o.matmul(x, wq[:rows], rows, K)
     t = time.perf_counter() - t0
-    byts = sum(alg_bytes(M, rows, K) for N, K, _, _ in host) * args.steps
+    byts = sum(alg_bytes(M, rows, K, 2 if args.y_dtype == "bf16" else 4) for N, K, _, _ in host) * args.steps
     flops = sum(2.0 * M * rows * K for N, K, _, _ in host) * args.steps
     unit = "GB/s" if M < 256 else "TFLOP/s"
     val = byts / t / 1e9 if M < 256 else flops / t / 1e12
@@ -469,8 +475,8 @@ def run_reference(args, rank, world, local):
             "n_gpus": world, "steps": args.steps, "warmup": warm,
             "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_name(args.workload, M, 1), "M": M,
-                       "shapes": {s: list(nk) for s, nk in shapes}},
+            "config": {"workload": workload_name(args.workload, M, ref_layers), "M": M,
+                       "shapes": {s: list(nk) for s, nk in shapes}, "y": args.y_dtype},
             "cpu_baseline": {"value": round(val, 4), "unit": unit, "cores": o.threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(val, 4), "unit": unit, "h2d_bytes_per_step": 0,

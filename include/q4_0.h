@@ -127,6 +127,27 @@ int q4_0_matmul_ws(const uint16_t *x, const uint8_t *wq, float *y,
                    int64_t M, int64_t N, int64_t K,
                    void *workspace, size_t workspace_bytes, void *stream);
 
+/* Element types of y for q4_0_matmul_ex. */
+#define Q4_0_Y_F32 0  /* float, as q4_0_matmul */
+#define Q4_0_Y_BF16 1 /* bfloat16: the fp32 result rounded to nearest even */
+
+/*
+ * q4_0_matmul_ex -- q4_0_matmul with a choice of output element type: y is
+ * [M][N] row-major of `y_type` (Q4_0_Y_F32 or Q4_0_Y_BF16; anything else is
+ * Q4_0_ERR_INVALID_ARG), 16-byte aligned.  Every kernel accumulates in fp32
+ * and rounds once at the store, so a Q4_0_Y_BF16 result equals the
+ * round-to-nearest-even bfloat16 of the Q4_0_Y_F32 result of the same call.
+ * Downstream layers that take bf16 activations read y directly, and the
+ * store writes half the bytes.  The pages leave the output type open; this
+ * is the bf16-output option of the epilogue.
+ * Workspace: as q4_0_matmul_ws; workspace NULL with workspace_bytes 0 makes
+ * the library take its own (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * Returns as q4_0_matmul_ws.
+ */
+int q4_0_matmul_ex(const uint16_t *x, const uint8_t *wq, void *y, int y_type,
+                   int64_t M, int64_t N, int64_t K,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * q4_0_gemv -- the decode kernels alone (what q4_0_matmul runs for
  * M <= 32).  Same arguments, layout and result contract as q4_0_matmul;

@@ -22,6 +22,10 @@ ERR_CUDA = -3
 ERR_DEVICE_TIMEOUT = -4
 ERR_WORKSPACE = -5
 
+# Output element types of q4_0_matmul_ex (include/q4_0.h).
+Y_F32 = 0
+Y_BF16 = 1
+
 # Every entry point the header declares, with its ctypes signature.
 _P, _I64, _SZ, _INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
 SIGNATURES = {
@@ -32,6 +36,7 @@ SIGNATURES = {
     "q4_0_matmul": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "q4_0_matmul_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "q4_0_matmul_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
+    "q4_0_matmul_ex": ([_P, _P, _P, _INT, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemv": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "q4_0_gemv_workspace_bytes": ([_I64, _I64], _SZ),
     "q4_0_gemv_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
@@ -120,7 +125,7 @@ def quantize(w: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Te
     return out
 
 
-def _mm_args(x, wq, N, K, out):
+def _mm_args(x, wq, N, K, out, out_dtype=torch.float32):
     _need(x, "x", torch.bfloat16, 2)
     _need(wq, "wq", torch.uint8, 2)
     M = x.shape[0]
@@ -129,8 +134,8 @@ def _mm_args(x, wq, N, K, out):
     if wq.numel() != weight_bytes(N, K):
         raise ValueError("wq does not hold an N x K Q4_0 matrix")
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    _need(out, "out", torch.float32, 2)
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _need(out, "out", out_dtype, 2)
     if tuple(out.shape) != (M, N):
         raise ValueError("out must be [M, N]")
     return M, out
@@ -147,9 +152,18 @@ def _workspace(nbytes, device, workspace):
 
 
 def matmul(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
-           workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
-    """y = x W^T: x bf16 [M, K], wq Q4_0 [N, K] -> fp32 [M, N] (the dispatcher)."""
-    M, out = _mm_args(x, wq, N, K, out)
+           workspace: torch.Tensor = None, stream=None, out_dtype=torch.float32) -> torch.Tensor:
+    """y = x W^T: x bf16 [M, K], wq Q4_0 [N, K] -> [M, N] fp32 (the dispatcher),
+    or bf16 with out_dtype=torch.bfloat16 (q4_0_matmul_ex)."""
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+    M, out = _mm_args(x, wq, N, K, out, out_dtype)
+    if out_dtype == torch.bfloat16:
+        ws, wsb = _workspace(int(lib().q4_0_matmul_workspace_bytes(M, N, K)), x.device, workspace)
+        _check(lib().q4_0_matmul_ex(x.data_ptr(), wq.data_ptr(), out.data_ptr(), Y_BF16, M, N, K,
+                                    ws.data_ptr() if ws is not None else None, wsb, _stream(stream)),
+               "q4_0_matmul_ex")
+        return out
     ws, wsb = _workspace(int(lib().q4_0_matmul_workspace_bytes(M, N, K)), x.device, workspace)
     _check(lib().q4_0_matmul_ws(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
                                 ws.data_ptr() if ws is not None else None, wsb, _stream(stream)),

@@ -167,7 +167,10 @@ size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return q4_0_gemm_workspace_bytes(M, N, K);
 }
 
-int q4_0_gemv_ws(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+namespace {
+// The decode and GEMM paths with the output element type as a flag (the
+// public entry points below are these with fp32 y, or q4_0_matmul_ex).
+int gemv_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
                  void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
@@ -177,27 +180,11 @@ int q4_0_gemv_ws(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int6
         return Q4_0_ERR_WORKSPACE;
     unsigned int *err = device_error_word();
     if (!err) return Q4_0_ERR_CUDA;
-    return from_cuda(launch_gemv(x, wq, y, M, N, K, need ? workspace : nullptr,
+    return from_cuda(launch_gemv(x, wq, y, ybf16, M, N, K, need ? workspace : nullptr,
                                  static_cast<cudaStream_t>(stream), err));
 }
 
-int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
-              void *stream) {
-    int st = check_matmul_args(x, wq, y, M, N, K);
-    if (st != Q4_0_OK) return st;
-    if (M > 32) return Q4_0_ERR_UNSUPPORTED;
-    const size_t bytes = gemv_workspace_bytes(M, K);
-    if (bytes == 0) return q4_0_gemv_ws(x, wq, y, M, N, K, nullptr, 0, stream);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    void *ws = nullptr;
-    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return Q4_0_ERR_CUDA;
-    st = q4_0_gemv_ws(x, wq, y, M, N, K, ws, bytes, stream);
-    const cudaError_t fe = cudaFreeAsync(ws, s);
-    if (st == Q4_0_OK && fe != cudaSuccess) st = Q4_0_ERR_CUDA;
-    return st;
-}
-
-int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+int gemm_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
               void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
@@ -210,30 +197,70 @@ int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t
     unsigned int *err = device_error_word();
     if (!err) return Q4_0_ERR_CUDA;
     return from_cuda(
-        launch_gemm(x, wq, y, M, N, K, workspace, splits, static_cast<cudaStream_t>(stream), err));
+        launch_gemm(x, wq, y, ybf16, M, N, K, workspace, splits, static_cast<cudaStream_t>(stream), err));
+}
+
+int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    int st = check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    if (M <= 32) return gemv_ws_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
+    return gemm_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
+}
+
+// As matmul_ws_impl with scratch taken by cudaMallocAsync on the stream.
+int matmul_alloc_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
+                      int64_t K, void *stream) {
+    int st = check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    const size_t bytes = q4_0_matmul_workspace_bytes(M, N, K);
+    if (bytes == 0) return matmul_ws_impl(x, wq, y, ybf16, M, N, K, nullptr, 0, stream);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return Q4_0_ERR_CUDA;
+    st = matmul_ws_impl(x, wq, y, ybf16, M, N, K, ws, bytes, stream);
+    const cudaError_t fe = cudaFreeAsync(ws, s);
+    if (st == Q4_0_OK && fe != cudaSuccess) st = Q4_0_ERR_CUDA;
+    return st;
+}
+}  // namespace
+
+int q4_0_gemv_ws(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+                 void *workspace, size_t workspace_bytes, void *stream) {
+    return gemv_ws_impl(x, wq, y, false, M, N, K, workspace, workspace_bytes, stream);
+}
+
+int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+              void *stream) {
+    int st = check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    if (M > 32) return Q4_0_ERR_UNSUPPORTED;
+    return matmul_alloc_impl(x, wq, y, false, M, N, K, stream);
+}
+
+int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+              void *workspace, size_t workspace_bytes, void *stream) {
+    return gemm_impl(x, wq, y, false, M, N, K, workspace, workspace_bytes, stream);
 }
 
 int q4_0_matmul_ws(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
                    void *workspace, size_t workspace_bytes, void *stream) {
-    int st = check_matmul_args(x, wq, y, M, N, K);
-    if (st != Q4_0_OK) return st;
-    if (M <= 32) return q4_0_gemv_ws(x, wq, y, M, N, K, workspace, workspace_bytes, stream);
-    return q4_0_gemm(x, wq, y, M, N, K, workspace, workspace_bytes, stream);
+    return matmul_ws_impl(x, wq, y, false, M, N, K, workspace, workspace_bytes, stream);
 }
 
 int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
                 void *stream) {
-    int st = check_matmul_args(x, wq, y, M, N, K);
-    if (st != Q4_0_OK) return st;
-    if (M <= 32) return q4_0_gemv(x, wq, y, M, N, K, stream);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t bytes = q4_0_gemm_workspace_bytes(M, N, K);
-    void *ws = nullptr;
-    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return Q4_0_ERR_CUDA;
-    st = q4_0_gemm(x, wq, y, M, N, K, ws, bytes, stream);
-    const cudaError_t fe = cudaFreeAsync(ws, s);
-    if (st == Q4_0_OK && fe != cudaSuccess) st = Q4_0_ERR_CUDA;
-    return st;
+    return matmul_alloc_impl(x, wq, y, false, M, N, K, stream);
+}
+
+int q4_0_matmul_ex(const uint16_t *x, const uint8_t *wq, void *y, int y_type, int64_t M, int64_t N, int64_t K,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    if (y_type != Q4_0_Y_F32 && y_type != Q4_0_Y_BF16) return Q4_0_ERR_INVALID_ARG;
+    float *yf = static_cast<float *>(y);
+    const bool bf16 = y_type == Q4_0_Y_BF16;
+    if (!workspace && workspace_bytes == 0 && q4_0_matmul_workspace_bytes(M, N, K) != 0)
+        return matmul_alloc_impl(x, wq, yf, bf16, M, N, K, stream);
+    return matmul_ws_impl(x, wq, yf, bf16, M, N, K, workspace, workspace_bytes, stream);
 }
 
 int q4_0_selftest_wait_timeout(int64_t limit_us, void *stream) {

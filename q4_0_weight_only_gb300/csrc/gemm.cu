@@ -94,9 +94,10 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__
     x16[i] = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// y = sum over splits of the partial tiles, in split order (deterministic).
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__restrict__ part, float4 *__restrict__ y,
-                                                            int64_t n4, int splits) {
+// y = sum over splits of the partial tiles, in split order (deterministic);
+// y is fp32, or bfloat16 rounded to nearest even when ybf16.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__restrict__ part, float *__restrict__ y,
+                                                            int64_t n4, int splits, int ybf16) {
     pdl_launch_dependents();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -109,7 +110,13 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__rest
         acc.z += v.z;
         acc.w += v.w;
     }
-    y[i] = acc;
+    if (ybf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        reinterpret_cast<uint2 *>(y)[i] =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+    } else {
+        reinterpret_cast<float4 *>(y)[i] = acc;
+    }
 }
 
 // One Q4_0 block -> 16 TMEM columns of packed binary16 pairs, each value
@@ -151,7 +158,7 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                float *__restrict__ y, float *__restrict__ part, int M, int N, int K, int TM,
+                float *__restrict__ y, float *__restrict__ part, int M, int N, int K, int TM, int ybf16,
                 unsigned int *err) {
     const GemmLayout Cfg(TM);
     extern __shared__ uint8_t smem_raw[];
@@ -175,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w_begin = (int)((int64_t)blockIdx.z * KW_all / gridDim.z);
     const int w_end = (int)((int64_t)(blockIdx.z + 1) * KW_all / gridDim.z);
     const int KWS = w_end - w_begin, KS = KWS * (kKW / kKB);
-    float *out = part ? part + (size_t)blockIdx.z * M * N : y;
+    float *out = part ? part + (size_t)blockIdx.z * M * N : nullptr;  // fp32 partial tile of a K split
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNW; ++i) {
@@ -320,7 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int m = m0 + c + j;
-                    if (c + j < TM && m < M && n < N) out[(int64_t)m * N + n] = __uint_as_float(v[j]);
+                    if (c + j < TM && m < M && n < N) {
+                        if (out)
+                            out[(int64_t)m * N + n] = __uint_as_float(v[j]);
+                        else
+                            store_y(y, (int64_t)m * N + n, __uint_as_float(v[j]), ybf16 != 0);
+                    }
                 }
             }
         }
@@ -359,8 +371,8 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, float *y, float *part, int64_t M,
-                      int64_t N, int64_t K, cudaStream_t s, unsigned int *err) {
+cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, float *y, bool ybf16, float *part,
+                      int64_t M, int64_t N, int64_t K, cudaStream_t s, unsigned int *err) {
     const GemmLayout Cfg(TM);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -390,11 +402,11 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, fl
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM), (unsigned)splits);
     e = launch_pdl(gemm_kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr,
-                   (int)M, (int)N, (int)K, TM, err);
+                   (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
     if (e != cudaSuccess || splits == 1) return e;
     const int64_t n4 = M * N / 4;
     return launch_pdl(splitk_reduce_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, s,
-                      reinterpret_cast<const float4 *>(part), reinterpret_cast<float4 *>(y), n4, splits);
+                      reinterpret_cast<const float4 *>(part), y, n4, splits, ybf16 ? 1 : 0);
 }
 
 }  // namespace
@@ -439,7 +451,7 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {
     return b;
 }
 
-cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, int splits, cudaStream_t s, unsigned int *err) {
     void *x16 = workspace;
     float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + x16_bytes(M, K));
@@ -451,7 +463,7 @@ cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t 
     if (e != cudaSuccess) return e;
     // fewest M tiles of at most 256 rows, then the smallest multiple of 16
     // that covers M in that many tiles
-    return launch_tm(tile_rows(M), splits < 1 ? 1 : splits, x16, wq, y, part, M, N, K, s, err);
+    return launch_tm(tile_rows(M), splits < 1 ? 1 : splits, x16, wq, y, ybf16, part, M, N, K, s, err);
 }
 
 }  // namespace q4_0

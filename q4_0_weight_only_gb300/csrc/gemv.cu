@@ -45,6 +45,7 @@ struct GemvArgs {
     int C;         // chunks per row
     int nb;        // blocks per row (K / 32)
     int mrows;     // valid x rows in this launch
+    int ybf16;     // y is bfloat16 (else fp32)
     uint32_t off_sx, off_ring, off_bars, off_part, off_flag;
 };
 
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = t / nrows, r = t - m * nrows;
         float s = 0.f;
         for (int c = 0; c < C; ++c) s += part[(r * C + c) * MT + m];
-        y[(int64_t)m * a.N + r0 + r] = s;
+        store_y(y, (int64_t)m * a.N + r0 + r, s, a.ybf16 != 0);
     }
 }
 
@@ -321,7 +322,7 @@ struct Limits {
 
 struct Args {
     int64_t N, K;
-    int P, c, T, R, S, rowbytes, H, mrows;
+    int P, c, T, R, S, rowbytes, H, mrows, ybf16;
     uint32_t stage_bytes, off_x, off_bars, off_part;
 };
 
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
         if (rr >= stage_rows(i)) continue;
         float sum = 0.f;
         for (int h = 0; h < a.H; ++h) sum += part[((size_t)lr * a.H + h) * MT + m];
-        y[(int64_t)m * a.N + stage_row0(i) + rr] = sum;
+        store_y(y, (int64_t)m * a.N + stage_row0(i) + rr, sum, a.ybf16 != 0);
     }
 }
 
@@ -645,7 +646,7 @@ Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
 }
 
 template <int MT>
-cudaError_t launch(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
+cudaError_t launch(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
                    int sms, cudaStream_t s, unsigned int *err, bool *done) {
     *done = false;
     const int grid = (int)(N < sms ? N : sms);
@@ -653,10 +654,11 @@ cudaError_t launch(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, in
     if (!p.ok) return cudaSuccess;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_dp4a_kernel<MT>), (int)p.smem);
     if (e != cudaSuccess) return e;
+    p.a.ybf16 = ybf16 ? 1 : 0;
     for (int64_t m0 = 0; m0 < M; m0 += MT) {
         p.a.mrows = (int)(M - m0 < MT ? M - m0 : MT);
         e = launch_pdl(gemv_dp4a_kernel<MT>, dim3(grid), dim3(p.threads), p.smem, s, x + m0 * K, wq,
-                       y + m0 * N, p.a, err);
+                       y_offset(y, m0 * N, ybf16), p.a, err);
         if (e != cudaSuccess) return e;
     }
     *done = true;
@@ -671,7 +673,7 @@ size_t gemv_workspace_bytes(int64_t M, int64_t K) {
     return M >= 3 && M <= 32 ? gemv_tc_workspace_bytes(M, K) : 0;
 }
 
-cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -682,12 +684,12 @@ cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t 
     const int grid = (int)grid64;
     if (M <= 2) {
         bool done = false;
-        e = M == 1 ? dp::launch<1>(x, wq, y, M, N, K, sms, s, err, &done)
-                   : dp::launch<2>(x, wq, y, M, N, K, sms, s, err, &done);
+        e = M == 1 ? dp::launch<1>(x, wq, y, ybf16, M, N, K, sms, s, err, &done)
+                   : dp::launch<2>(x, wq, y, ybf16, M, N, K, sms, s, err, &done);
         if (e != cudaSuccess || done) return e;
     } else {
         // three or more rows of x: the dot product moves to the tensor cores
-        return launch_gemv_tc(x, wq, y, M, N, K, workspace, s, err);
+        return launch_gemv_tc(x, wq, y, ybf16, M, N, K, workspace, s, err);
     }
     // rows of x per launch: the largest power of two <= 8 that covers M (or
     // fits shared memory); each launch streams the weights once
@@ -698,8 +700,9 @@ cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t 
     for (int64_t m0 = 0; m0 < M; m0 += mt) {
         GemvPlan p = plan_gemv(mt, N, K, grid);
         p.args.mrows = (int)((M - m0) < mt ? (M - m0) : mt);
+        p.args.ybf16 = ybf16 ? 1 : 0;
         const uint16_t *xm = x + m0 * K;
-        float *ym = y + m0 * N;
+        float *ym = y_offset(y, m0 * N, ybf16);
         switch (mt) {
             case 1: e = launch_mt<1>(xm, wq, ym, p, grid, s, err); break;
             case 2: e = launch_mt<2>(xm, wq, ym, p, grid, s, err); break;

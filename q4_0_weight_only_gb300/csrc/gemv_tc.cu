@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) x_tiles_kernel(const uint16_t *__restrict
 template <int TM>
 __global__ void __launch_bounds__(kThreads, 2)
     gemv_tc_kernel(const uint4 *__restrict__ xt, const __grid_constant__ CUtensorMap wmap,
-                   float *__restrict__ y, int M, int N, int K, unsigned int *err) {
+                   float *__restrict__ y, int M, int N, int K, int ybf16, unsigned int *err) {
     using C = Cfg<TM>;
     constexpr int kNX = C::kNX;
     extern __shared__ uint8_t smem_raw[];
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float sum = 0.f;
 #pragma unroll
                 for (int q = 0; q < kMaxCluster; ++q) sum += v[q];  // rank order
-                y[(int64_t)m * N + n] = sum;
+                store_y(y, (int64_t)m * N + n, sum, ybf16 != 0);
             }
         }
     }
@@ -401,8 +401,8 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int TM>
-cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N, int64_t K,
-                      void *xtiles, cudaStream_t s, unsigned int *err) {
+cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
+                      int64_t K, void *xtiles, cudaStream_t s, unsigned int *err) {
     using C = Cfg<TM>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -437,7 +437,7 @@ cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M,
     if (e != cudaSuccess) return e;
     return launch_pdl_cluster(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads),
                               C::kSmem, s, (unsigned)S, static_cast<const uint4 *>(xtiles), wmap, y, (int)M,
-                              (int)N, (int)K, err);
+                              (int)N, (int)K, ybf16 ? 1 : 0, err);
 }
 
 }  // namespace
@@ -447,10 +447,10 @@ size_t gemv_tc_workspace_bytes(int64_t M, int64_t K) {
     return (size_t)(tm * K * 2);
 }
 
-cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                            int64_t K, void *xtiles, cudaStream_t s, unsigned int *err) {
-    if (M <= 16) return launch_tm<16>(x, wq, y, M, N, K, xtiles, s, err);
-    return launch_tm<32>(x, wq, y, M, N, K, xtiles, s, err);
+    if (M <= 16) return launch_tm<16>(x, wq, y, ybf16, M, N, K, xtiles, s, err);
+    return launch_tm<32>(x, wq, y, ybf16, M, N, K, xtiles, s, err);
 }
 
 }  // namespace q4_0

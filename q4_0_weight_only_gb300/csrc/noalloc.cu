@@ -75,6 +75,6 @@ extern "C" int q4_0_gemm_noalloc(const uint16_t *x, const uint8_t *wq, float *y,
     unsigned int *err = q4_0::device_error_word();
     if (!err) return Q4_0_ERR_CUDA;
     const cudaError_t e =
-        q4_0::launch_gemm(x, wq, y, M, N, K, scratch, 1, static_cast<cudaStream_t>(stream), err);
+        q4_0::launch_gemm(x, wq, y, false, M, N, K, scratch, 1, static_cast<cudaStream_t>(stream), err);
     return e == cudaSuccess ? Q4_0_OK : Q4_0_ERR_CUDA;
 }

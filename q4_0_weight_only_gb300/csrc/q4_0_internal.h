@@ -59,18 +59,24 @@ unsigned int *device_error_word();
 cudaError_t launch_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, cudaStream_t s,
                             unsigned int *err);
 
+// y is fp32, or bfloat16 when `ybf16` (passed as float *; element i of row
+// m at index m * N + i of the element type).
+inline float *y_offset(float *y, int64_t elems, bool ybf16) {
+    return ybf16 ? reinterpret_cast<float *>(reinterpret_cast<uint16_t *>(y) + elems) : y + elems;
+}
+
 // Decode GEMV for M <= 32 (x, y point at row 0; row strides K and N).
 // `workspace` (256-byte aligned, gemv_workspace_bytes(M, K) bytes) is used for
 // 3 <= M <= 32 only.
 size_t gemv_workspace_bytes(int64_t M, int64_t K);
-cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, cudaStream_t s, unsigned int *err);
 
 // Tensor-core decode for 3 <= M <= 32: x rounded once into binary16 MMA
 // tiles in `xtiles` (gemv_tc_workspace_bytes(M, K) bytes), then split-K over
 // a thread-block cluster.
 size_t gemv_tc_workspace_bytes(int64_t M, int64_t K);
-cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                            int64_t K, void *xtiles, cudaStream_t s, unsigned int *err);
 
 // tcgen05 GEMM.  `workspace` holds x rounded to binary16 and, when K is
@@ -78,7 +84,7 @@ cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, int64
 // splits) bytes.  gemm_splits picks the split for a device with `sms` SMs.
 int gemm_splits(int64_t M, int64_t N, int64_t K, int sms);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
-cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t N,
+cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, int splits, cudaStream_t s, unsigned int *err);
 
 }  // namespace q4_0

@@ -3,6 +3,7 @@
 // instructions used by the Q4_0 kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -170,6 +171,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *m
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------- output
+
+// One element of y: fp32, or bfloat16 rounded to nearest even when `bf16`.
+__device__ __forceinline__ void store_y(float *y, int64_t i, float v, bool bf16) {
+    if (bf16)
+        reinterpret_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
+    else
+        y[i] = v;
 }
 
 // -------------------------------------------------------------- tcgen05

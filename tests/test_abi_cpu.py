@@ -77,6 +77,8 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.q4_0_matmul(good, good, good, 1, 1, 96, None) == -2     # K % 256
     assert lib.q4_0_matmul(P((1 << 20) + 8), good, good, 1, 1, 256, None) == -1  # misaligned
     assert lib.q4_0_gemv(good, good, good, 33, 1, 256, None) == -2
+    assert lib.q4_0_matmul_ex(good, good, good, 7, 1, 1, 256, None, 0, None) == -1   # unknown y type
+    assert lib.q4_0_matmul_ex(good, good, good, 1, 1, 1, 96, None, 0, None) == -2    # K % 256
     assert lib.q4_0_gemv_ws(good, good, good, 16, 1, 256, None, 0, None) == -5
     assert lib.q4_0_gemv_ws(good, good, good, 16, 1, 256, P((1 << 20) + 16), 1 << 20, None) == -5
     assert lib.q4_0_gemv_ws(good, good, good, 16, 1, 256, good, 16 * 256 * 2 - 1, None) == -5

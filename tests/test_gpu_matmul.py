@@ -192,6 +192,36 @@ def test_gemv_scratch_paths_agree():
     assert q4.device_error() == 0
 
 
+BF16_OUT = [(1, 300, 2048),        # integer-dot decode
+            (1, 200, 1280),        # general-K decode
+            (2, 129, 1024),        # integer-dot decode, two rows
+            (3, 300, 1536), (16, 512, 1024), (32, 256, 3072),   # tensor-core decode
+            (64, 1000, 1280),      # GEMM
+            (272, 384, 5120)]      # GEMM with a K split and the partial-tile sum
+
+
+@pytest.mark.parametrize("M,N,K", BF16_OUT)
+def test_bf16_output_is_the_rounded_f32_output(M, N, K):
+    """q4_0_matmul_ex with bf16 y: every path rounds its fp32 result once
+    (nearest even) at the store, so the bits equal bf16(fp32 y) of the same
+    call, with the caller's workspace and with library-allocated scratch; and
+    the result meets the oracle tolerance."""
+    q4 = lib()
+    x, wq = case(9100 + M, M, N, K, outlier_blocks=0.05, act_outliers=0.01)
+    xd, wd = x_dev(x), wq_dev(wq)
+    y32 = q4.matmul(xd, wd, N, K)
+    y16 = q4.matmul(xd, wd, N, K, out_dtype=torch.bfloat16)
+    assert y16.dtype == torch.bfloat16
+    assert torch.equal(y16.view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))
+    alloc = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = q4.lib().q4_0_matmul_ex(xd.data_ptr(), wd.data_ptr(), alloc.data_ptr(), q4.Y_BF16, M, N, K,
+                                 None, 0, None)
+    assert st == q4.OK
+    assert torch.equal(alloc.view(torch.int16), y16.view(torch.int16))
+    check_full(y16.float(), x, wq, N, K)
+    assert q4.device_error() == 0
+
+
 # --------------------------------------------------------- workload sizes
 
 def test_pr1():
