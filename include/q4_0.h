@@ -89,8 +89,12 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
  *   x   : bf16 bit patterns [M][K] row-major, device (the __nv_bfloat16 type).
  *   wq  : Q4_0 matrix W [N][K] as above, device.
  *   y   : float [M][N] row-major, device, fully overwritten (no accumulate).
- *   M, N, K: M >= 1, N >= 1, K >= 256, K % 256 == 0 (K % 32 != 0 is
- *         INVALID_ARG; K % 32 == 0 but K % 256 != 0 is UNSUPPORTED).
+ *   M, N, K: M >= 1, N >= 1, K >= 32, K % 32 == 0 (else INVALID_ARG).
+ *         K % 256 != 0 is served by copying W and x, zero-padded to K
+ *         rounded up to 256, into the scratch first (one extra pass over W;
+ *         the extra blocks and elements are zero, so y is unchanged).  The
+ *         kernel-alone entry points below (q4_0_gemv*, q4_0_gemm*) need
+ *         K % 256 == 0 and return UNSUPPORTED otherwise.
  * y[m][n] = sum_k d(n,k) * (q(n,k) - 8) * x[m][k], accumulated in fp32.
  * Dispatch: M <= 2 runs the decode GEMV on CUDA cores (exact integer dot
  * products per 32-weight block on 15-bit fixed-point x, fp32 across blocks);
@@ -110,7 +114,8 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
 int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y,
                 int64_t M, int64_t N, int64_t K, void *stream);
 
-/* Scratch bytes q4_0_matmul needs for these sizes (0 for M <= 2). */
+/* Scratch bytes q4_0_matmul needs for these sizes (0 for M <= 2 when
+ * K % 256 == 0; for other K it includes the zero-padded copies of W and x). */
 size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "lib", "libq4_0.so")
-SOURCES = ["api.cu", "quantize.cu", "gemv.cu", "gemv_tc.cu", "gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemv.cu", "gemv_tc.cu", "gemm.cu", "noalloc.cu", "pad.cu"]
 HEADERS = ["q4_0_internal.h", "q4_0_ptx.cuh"]
 PUBLIC_HEADER = os.path.join(os.path.dirname(HERE), "include", "q4_0.h")
 

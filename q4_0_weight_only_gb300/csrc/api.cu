@@ -97,12 +97,14 @@ namespace {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Common validation of a matmul call.
+// `any_k`: K % 32 == 0 is enough (the dispatcher pads other K to a multiple
+// of 256); the kernel-alone entry points need K % 256 == 0.
 int check_matmul_args(const void *x, const void *wq, const void *y, int64_t M, int64_t N,
-                      int64_t K) {
+                      int64_t K, bool any_k = false) {
     if (!x || !wq || !y) return Q4_0_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return Q4_0_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(wq) || !aligned16(y)) return Q4_0_ERR_INVALID_ARG;
-    if (K % 256 != 0) return Q4_0_ERR_UNSUPPORTED;
+    if (K % 256 != 0 && !any_k) return Q4_0_ERR_UNSUPPORTED;
     // keep every index and TMA coordinate in 32-bit range
     if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 24)) return Q4_0_ERR_UNSUPPORTED;
     if (M * K > (1ll << 40) || N * K > (1ll << 40) || M * N > (1ll << 40))
@@ -163,8 +165,12 @@ size_t q4_0_gemv_workspace_bytes(int64_t M, int64_t K) {
 }
 
 size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    if (M <= 32) return q4_0_gemv_workspace_bytes(M, K);
-    return q4_0_gemm_workspace_bytes(M, N, K);
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return 0;
+    // other K: the zero-padded copies of W and x, then the padded problem's own
+    const size_t pad = pad_bytes(M, N, K);
+    const int64_t kp = padded_k(K);
+    if (M <= 32) return pad + q4_0_gemv_workspace_bytes(M, kp);
+    return pad + q4_0_gemm_workspace_bytes(M, N, kp);
 }
 
 namespace {
@@ -202,8 +208,24 @@ int gemm_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_
 
 int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
                    void *workspace, size_t workspace_bytes, void *stream) {
-    int st = check_matmul_args(x, wq, y, M, N, K);
+    int st = check_matmul_args(x, wq, y, M, N, K, true);
     if (st != Q4_0_OK) return st;
+    if (K % 256 != 0) {
+        // copy W and x, zero-padded to a multiple of 256, then run the padded problem
+        const size_t pad = pad_bytes(M, N, K);
+        if (!workspace || workspace_bytes < q4_0_matmul_workspace_bytes(M, N, K) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return Q4_0_ERR_WORKSPACE;
+        uint16_t *xp = nullptr;
+        uint8_t *wqp = nullptr;
+        if (launch_pad(x, wq, M, N, K, workspace, &xp, &wqp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return Q4_0_ERR_CUDA;
+        void *rest = static_cast<uint8_t *>(workspace) + pad;
+        const size_t rest_bytes = workspace_bytes - pad;
+        const int64_t kp = padded_k(K);
+        if (M <= 32) return gemv_ws_impl(xp, wqp, y, ybf16, M, N, kp, rest_bytes ? rest : nullptr, rest_bytes, stream);
+        return gemm_impl(xp, wqp, y, ybf16, M, N, kp, rest, rest_bytes, stream);
+    }
     if (M <= 32) return gemv_ws_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
     return gemm_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
 }
@@ -211,7 +233,7 @@ int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, i
 // As matmul_ws_impl with scratch taken by cudaMallocAsync on the stream.
 int matmul_alloc_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                       int64_t K, void *stream) {
-    int st = check_matmul_args(x, wq, y, M, N, K);
+    int st = check_matmul_args(x, wq, y, M, N, K, true);
     if (st != Q4_0_OK) return st;
     const size_t bytes = q4_0_matmul_workspace_bytes(M, N, K);
     if (bytes == 0) return matmul_ws_impl(x, wq, y, ybf16, M, N, K, nullptr, 0, stream);

@@ -79,6 +79,15 @@ size_t gemv_tc_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                            int64_t K, void *xtiles, cudaStream_t s, unsigned int *err);
 
+// K % 32 == 0 but K % 256 != 0: W and x copied, zero-padded to K rounded up
+// to 256 (padded_k), into the front of `workspace` (pad_bytes(M, N, K)
+// bytes, 256-byte aligned); *xp and *wqp point at the copies.  Plain stream
+// order (see pad.cu).
+int64_t padded_k(int64_t K);
+size_t pad_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_pad(const uint16_t *x, const uint8_t *wq, int64_t M, int64_t N, int64_t K, void *workspace,
+                       uint16_t **xp, uint8_t **wqp, cudaStream_t s);
+
 // tcgen05 GEMM.  `workspace` holds x rounded to binary16 and, when K is
 // split (splits > 1), the fp32 partial tiles: gemm_workspace_bytes(M, N, K,
 // splits) bytes.  gemm_splits picks the split for a device with `sms` SMs.

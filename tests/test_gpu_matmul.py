@@ -192,6 +192,25 @@ def test_gemv_scratch_paths_agree():
     assert q4.device_error() == 0
 
 
+GENERAL_K = [(1, 300, 32), (1, 257, 96), (2, 100, 288), (1, 1000, 5152),   # decode kernels
+             (3, 64, 160), (16, 300, 1056), (32, 129, 2080),                   # tensor-core decode
+             (64, 300, 800), (300, 520, 1312)]                                 # GEMM
+
+
+@pytest.mark.parametrize("M,N,K", GENERAL_K)
+def test_general_k(M, N, K):
+    """K % 32 == 0 but not a multiple of 256: the dispatcher copies W and x,
+    zero-padded, into its scratch and runs the padded problem; results meet
+    the oracle tolerance and the allocating path gives the same bits."""
+    q4 = lib()
+    x, wq = case(9300 + M * 3 + K, M, N, K, outlier_blocks=0.05, act_outliers=0.01)
+    xd, wd = x_dev(x), wq_dev(wq)
+    y = q4.matmul(xd, wd, N, K)
+    check_full(y, x, wq, N, K)
+    assert torch.equal(q4.matmul_alloc(xd, wd, N, K), y)
+    assert q4.device_error() == 0
+
+
 BF16_OUT = [(1, 300, 2048),        # integer-dot decode
             (1, 200, 1280),        # general-K decode
             (2, 129, 1024),        # integer-dot decode, two rows
