@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <mutex>
+#include <type_traits>
 
 #include "q4_0_internal.h"
 #include "q4_0_ptx.cuh"
@@ -280,55 +281,68 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int quad = warp & 3, half = (warp - 2) >> 2;
         const int r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        bool ok = true;
-        for (int ws = 0; ws < nW && ok; ++ws) {
-            const int wsl = ws % kNW;
-            ok = __all_sync(0xffffffffu, mbar_wait(&w_full[wsl], (ws / kNW) & 1, abort_flag, err));
-            if (!ok) break;
-            // this warp's half of the row (bytes 72h .. 72h + 71) with five
-            // 16-byte loads from byte 64h: a 144-byte row stride puts the eight
-            // lanes of each load phase on distinct 16-byte bank groups, where
-            // 4-byte loads would conflict four ways; half 1 drops the first two
-            // words (warp-uniform selects keep every register index static)
-            const uint4 *row = reinterpret_cast<const uint4 *>(wring + wsl * kWStageBytes + r * kWRowBytes + 64 * half);
-            uint32_t rw[20];
+        // the half is a compile-time constant inside the loop (one copy per
+        // half, chosen per warp), so register indices stay static without
+        // selects; ring slots and phases advance incrementally (A slot
+        // s = 2 ws + half steps by two through a ring of three)
+        auto dequant = [&](auto half_c) -> bool {
+            constexpr int H = decltype(half_c)::value;
+            int wsl = 0, asl = H;
+            uint32_t wph = 0, aph = 0;
+            for (int ws = 0; ws < nW; ++ws) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&w_full[wsl], wph, abort_flag, err))) return false;
+                // this warp's half of the row (bytes 72h .. 72h + 71) with five
+                // 16-byte loads from byte 64h: a 144-byte row stride puts the
+                // eight lanes of each load phase on distinct 16-byte bank groups,
+                // where 4-byte loads would conflict four ways; half 1 skips the
+                // first two words
+                const uint4 *row =
+                    reinterpret_cast<const uint4 *>(wring + wsl * kWStageBytes + r * kWRowBytes + 64 * H);
+                uint32_t rw[20];
 #pragma unroll
-            for (int i = 0; i < 5; ++i) {
-                const uint4 q = row[i];
-                rw[4 * i + 0] = q.x;
-                rw[4 * i + 1] = q.y;
-                rw[4 * i + 2] = q.z;
-                rw[4 * i + 3] = q.w;
+                for (int i = 0; i < 5; ++i) {
+                    const uint4 q = row[i];
+                    rw[4 * i + 0] = q.x;
+                    rw[4 * i + 1] = q.y;
+                    rw[4 * i + 2] = q.z;
+                    rw[4 * i + 3] = q.w;
+                }
+                __syncwarp();  // every lane holds its part of the stage: release it
+                if (lane == 0) mbar_arrive(&w_empty[wsl]);
+                // A slot (stage, half): 128 k = two 64-k pieces of 32 columns
+                if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[asl], aph ^ 1, abort_flag, err))) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t *wv = rw + 2 * H + 9 * j;
+                    const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
+                                            __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
+                    const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+                    uint32_t cols[32];
+                    uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols);
+                    uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols + 16);
+                    dequant_block16(wv[0] & 0xFFFFu, Q0, lo);
+                    dequant_block16(wv[4] >> 16, Q1, hi);
+                    tmem_st32(a_tmem + lane_base + asl * (kKB / 2) + j * 32, cols);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();  // every lane's stores are done
+                if (lane == 0) mbar_arrive(&a_full[asl]);
+                if (++wsl == kNW) {
+                    wsl = 0;
+                    wph ^= 1;
+                }
+                asl += kSubs;
+                if (asl >= kNA) {
+                    asl -= kNA;
+                    aph ^= 1;
+                }
             }
-#pragma unroll
-            for (int i = 0; i < 18; ++i) rw[i] = half ? rw[i + 2] : rw[i];
-            __syncwarp();  // every lane holds its part of the stage: release it
-            if (lane == 0) mbar_arrive(&w_empty[wsl]);
-            // A slot s = (stage, half): 128 k = two 64-k pieces of 32 columns
-            const int s = ws * kSubs + half, asl = s % kNA;
-            ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                uint32_t wv[9];
-#pragma unroll
-                for (int i = 0; i < 9; ++i) wv[i] = rw[9 * j + i];
-                const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
-                                        __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
-                const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
-                uint32_t cols[32];
-                uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols);
-                uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols + 16);
-                dequant_block16(wv[0] & 0xFFFFu, Q0, lo);
-                dequant_block16(wv[4] >> 16, Q1, hi);
-                tmem_st32(a_tmem + lane_base + asl * (kKB / 2) + j * 32, cols);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();  // every lane's stores are done
-            if (lane == 0) mbar_arrive(&a_full[asl]);
-        }
+            return true;
+        };
+        static_assert(kSubs < kNA, "the A slot advances by kSubs and wraps at most once per stage");
+        bool ok = half ? dequant(std::integral_constant<int, 1>{}) : dequant(std::integral_constant<int, 0>{});
         // epilogue (warps 2..5 cover the four lane quarters): D -> partial tile
         if (half == 0) {
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));
