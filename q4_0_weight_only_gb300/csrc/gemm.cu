@@ -279,7 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the row's 144 bytes with nine 16-byte loads: with a 144-byte row
             // stride the eight lanes of each load phase hit distinct 16-byte
             // bank groups (4-byte loads would conflict four ways).  The stage
-            // is free again once every lane holds its row.
+            // goes back to the producer once every lane has used its row (after
+            // the last sub-slot): the next TMA fill of the slot is an
+            // async-proxy write and must not overtake shared loads in flight.
             const uint4 *row = reinterpret_cast<const uint4 *>(wring + wsl * kWStageBytes + r * kWRowBytes);
             uint32_t rw[36];
 #pragma unroll
@@ -290,8 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rw[4 * i + 2] = q.z;
                 rw[4 * i + 3] = q.w;
             }
-            __syncwarp();  // every lane's reads of the stage are done
-            if (lane == 0) mbar_arrive(&w_empty[wsl]);
 #pragma unroll
             for (int sub = 0; sub < kKW / kKB; ++sub) {
                 const int s = ws * (kKW / kKB) + sub, asl = s % kNA;
@@ -314,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();  // every lane's stores are done
                 if (lane == 0) mbar_arrive(&a_full[asl]);
             }
+            if (lane == 0) mbar_arrive(&w_empty[wsl]);
         }
         // epilogue: D[row r][column m] -> y[m][n0 + r]
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));

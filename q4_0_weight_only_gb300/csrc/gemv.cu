@@ -311,11 +311,15 @@ constexpr size_t kSmemLimit = 227 * 1024;
 // ---------------------------------------------------------------------------
 namespace dp {
 
-// One CTA per SM holding x in registers: as many threads as the register
-// file allows without spills.
+// One CTA per SM holding x in registers.  With one row of x a thread owns
+// G = 2 block pairs of a row (the per-stage overhead -- wait, release,
+// reduction, partial store -- is paid once per 128 weights); with two rows
+// the x registers of one pair per thread are what the register file allows.
 template <int MT>
 struct Limits {
-    static constexpr int kThreads = MT == 1 ? 896 : 640;
+    static constexpr int kG = MT == 1 ? 2 : 1;       // block pairs per thread
+    static constexpr int kRed = 16 / kG;              // lanes per partial (P / 16 partials per row)
+    static constexpr int kThreads = MT == 1 ? 448 : 640;
     static constexpr int kCtasPerSm = 1;
     static constexpr size_t kSmem = 227 * 1024;
 };
@@ -350,49 +354,48 @@ __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-// Eight elements (part `part` of block b of x row m) -> fixed point, written
-// into the pair record; the four threads of a block (consecutive lanes)
-// agree on the block's exponent and sum through shuffles.  `live` is false
-// for lanes past the end (they still take part in the shuffles).
+// Sixteen elements (half `part` of block b of x row m) -> fixed point,
+// written into the pair record; the two threads of a block (consecutive
+// lanes) agree on the block's exponent and sum through a shuffle.  `live` is
+// false for lanes past the end (they still take part in the shuffles).
 __device__ __forceinline__ void convert_part(const uint16_t *__restrict__ xrow, int b, int part,
                                              bool live, uint32_t *__restrict__ rec) {
-    float xv[8];
+    float xv[16];
     if (live && xrow) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(xrow + (int64_t)b * 32) + part);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+        const uint4 *src = reinterpret_cast<const uint4 *>(xrow + (int64_t)b * 32) + 2 * part;
+        const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+        const uint32_t w8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            xv[2 * h] = __uint_as_float(w4[h] << 16);
-            xv[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
+        for (int h = 0; h < 8; ++h) {
+            xv[2 * h] = __uint_as_float(w8[h] << 16);
+            xv[2 * h + 1] = __uint_as_float(w8[h] & 0xFFFF0000u);
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) xv[j] = 0.f;
+        for (int j = 0; j < 16; ++j) xv[j] = 0.f;
     }
     float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(xv[j]));
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(xv[j]));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     int e = 0;
     if (amax > 0.f) {
         frexpf(amax, &e);
         e = max(-100, min(127, e));
     }
     const float up = amax > 0.f ? ldexpf(1.0f, 14 - e) : 0.f;
-    int X[8], sum = 0;
+    int X[16], sum = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 16; ++j) {
         X[j] = __float2int_rn(xv[j] * up);
         sum += X[j];
     }
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     if (!live) return;
     const int blk = b & 1;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int wd = 2 * part + h;  // word: elements 4 wd .. 4 wd + 3
+    for (int h = 0; h < 4; ++h) {
+        const int wd = 4 * part + h;  // word: elements 4 wd .. 4 wd + 3
         const int *Xw = X + 4 * h;
         // bytes 1 (high) and 0 (low) of the four 16-bit fixed-point values
         rec[blk * 8 + wd] = __byte_perm(__byte_perm(Xw[0], Xw[1], 0x0051), __byte_perm(Xw[2], Xw[3], 0x0051), 0x5410);
@@ -509,46 +512,57 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
     // x -> fixed point in shared memory, once per CTA (overlaps the first copies)
     pdl_wait();
     const int nb = 2 * a.P;
-    const int nparts = 4 * MT * nb;  // four threads per 32-element block
+    const int nparts = 2 * MT * nb;  // two threads per 32-element block
     for (int t0 = tid - lane; t0 < nparts; t0 += a.T) {  // warp-uniform trip count
         const int t = t0 + lane;
         const bool live = t < nparts;
         const int q = live ? t : nparts - 1;
-        const int blk_id = q >> 2, part = q & 3;
+        const int blk_id = q >> 1, part = q & 1;
         const int m = blk_id / nb, b = blk_id - m * nb;
         convert_part(m < a.mrows ? x + (int64_t)m * a.K : nullptr, b, part, live,
                      xsm + ((size_t)m * a.P + (b >> 1)) * kPairWords);
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(a.T) : "memory");
+    named_bar_sync(1, a.T);
     if (tid == 0) mbar_arrive(xready);
 
-    const int pc = tid % a.P, rs = tid / a.P;
+    // thread (rs, tc) owns block pairs tc + g TPR (g < G) of row slot rs
+    constexpr int G = Limits<MT>::kG, kRed = Limits<MT>::kRed;
+    const int tpr = a.P / G;
+    const int tc = tid % tpr, rs = tid / tpr;
     const bool active = rs < a.c;
-    XReg<MT> xr;
+    XReg<MT> xr[G];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        const uint4 *rec = reinterpret_cast<const uint4 *>(xsm + ((size_t)m * a.P + pc) * kPairWords);
+    for (int g = 0; g < G; ++g) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 u = rec[i], w = rec[4 + i];
-            xr.h[m][4 * i] = u.x; xr.h[m][4 * i + 1] = u.y; xr.h[m][4 * i + 2] = u.z; xr.h[m][4 * i + 3] = u.w;
-            xr.l[m][4 * i] = w.x; xr.l[m][4 * i + 1] = w.y; xr.l[m][4 * i + 2] = w.z; xr.l[m][4 * i + 3] = w.w;
+        for (int m = 0; m < MT; ++m) {
+            const uint4 *rec =
+                reinterpret_cast<const uint4 *>(xsm + ((size_t)m * a.P + tc + g * tpr) * kPairWords);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 u = rec[i], w = rec[4 + i];
+                xr[g].h[m][4 * i] = u.x; xr[g].h[m][4 * i + 1] = u.y;
+                xr[g].h[m][4 * i + 2] = u.z; xr[g].h[m][4 * i + 3] = u.w;
+                xr[g].l[m][4 * i] = w.x; xr[g].l[m][4 * i + 1] = w.y;
+                xr[g].l[m][4 * i + 2] = w.z; xr[g].l[m][4 * i + 3] = w.w;
+            }
+            const uint4 t = rec[8];
+            xr[g].ncorr[m][0] = (int)t.x;
+            xr[g].ncorr[m][1] = (int)t.y;
+            xr[g].xs[m][0] = __uint_as_float(t.z);
+            xr[g].xs[m][1] = __uint_as_float(t.w);
         }
-        const uint4 t = rec[8];
-        xr.ncorr[m][0] = (int)t.x;
-        xr.ncorr[m][1] = (int)t.y;
-        xr.xs[m][0] = __uint_as_float(t.z);
-        xr.xs[m][1] = __uint_as_float(t.w);
     }
 
-    // one row per thread per stage: copy the row's block pair to registers,
-    // release the stage to the producer at once, then compute.  The loop is
+    // one row per thread per stage: copy the row's block pairs to registers,
+    // compute, then release the stage to the producer (only once the loaded
+    // words have been used: the next bulk fill of the slot is an async-proxy
+    // write and must not overtake shared loads still in flight).  The loop is
     // issue-bound at one pair per thread per stage, so the ring slot, its
     // phase and the partials' address advance incrementally: a runtime
     // division per stage (i % S, i / S) cost about a tenth of the rate.
     const int last_rows = (int)(r1 - r0 - (int64_t)(nst - 1) * a.R);
-    const uint8_t *my_row = smem + (size_t)rs * a.rowbytes + pc * 36;
-    float *my_part = part + ((size_t)rs * a.H + (pc >> 4)) * MT;
+    const uint8_t *my_row = smem + (size_t)rs * a.rowbytes + tc * 36;
+    float *my_part = part + ((size_t)rs * a.H + tc / kRed) * MT;
     const int part_step = a.R * a.H * MT;
     int s = 0;
     uint32_t ph = 0;
@@ -557,34 +571,40 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
         if (!__all_sync(0xffffffffu, ok)) break;
         const int rows = i == nst - 1 ? last_rows : a.R;
         const bool valid = active && rs < rows;
-        uint32_t wv[9];
+        uint32_t wv[G][9];
         if (valid) {
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(my_row + (uint32_t)s * a.stage_bytes);
 #pragma unroll
-            for (int k = 0; k < 9; ++k) wv[k] = src[k];
+            for (int g = 0; g < G; ++g) {
+                const uint32_t *src =
+                    reinterpret_cast<const uint32_t *>(my_row + (uint32_t)s * a.stage_bytes + g * tpr * 36);
+#pragma unroll
+                for (int k = 0; k < 9; ++k) wv[g][k] = src[k];
+            }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
         float v[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) v[m] = 0.f;
         if (valid) {
-            const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
-                                    __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
-            const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
-            block_dp<MT>(wv[0] & 0xFFFFu, Q0, xr, 0, v);
-            block_dp<MT>(wv[4] >> 16, Q1, xr, 1, v);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t *w = wv[g];
+                const uint32_t Q0[4] = {__funnelshift_r(w[0], w[1], 16), __funnelshift_r(w[1], w[2], 16),
+                                        __funnelshift_r(w[2], w[3], 16), __funnelshift_r(w[3], w[4], 16)};
+                const uint32_t Q1[4] = {w[5], w[6], w[7], w[8]};
+                block_dp<MT>(w[0] & 0xFFFFu, Q0, xr[g], 0, v);
+                block_dp<MT>(w[4] >> 16, Q1, xr[g], 1, v);
+            }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             float t = v[m];
-            t += __shfl_xor_sync(0xffffffffu, t, 8);
-            t += __shfl_xor_sync(0xffffffffu, t, 4);
-            t += __shfl_xor_sync(0xffffffffu, t, 2);
-            t += __shfl_xor_sync(0xffffffffu, t, 1);
+#pragma unroll
+            for (int o = kRed / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
             v[m] = t;
         }
-        if (valid && (lane & 15) == 0) {
+        if (valid && (lane & (kRed - 1)) == 0) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) my_part[m] = v[m];
         }
@@ -594,8 +614,8 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
             ph ^= 1;
         }
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(a.T) : "memory");
-    // fixed-order sum over half-warp partials; consecutive threads write
+    named_bar_sync(1, a.T);
+    // fixed-order sum over the P / 16 partials of a row; consecutive threads write
     // consecutive rows of a stage
     const int local_rows = nst * a.R;
     for (int t = tid; t < local_rows * a.mrows; t += a.T) {
@@ -615,8 +635,8 @@ struct Plan {
     bool ok;
 };
 
-// One CTA per SM: c row slots of P threads (P = K / 64 block pairs), a
-// producer warp, and as many row stages of about 20 KB as shared memory holds.
+// One CTA per SM: c row slots of P / G threads (P = K / 64 block pairs), a
+// producer warp, and as many row stages of about 29 KB as shared memory holds.
 Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
     Plan p{};
     Args &a = p.a;
@@ -628,8 +648,9 @@ Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
     const int max_threads = mt == 1 ? Limits<1>::kThreads : Limits<2>::kThreads;
     const size_t smem_limit = mt == 1 ? Limits<1>::kSmem : Limits<2>::kSmem;
     const int budget = max_threads - 32;
-    a.c = max(1, budget / a.P);  // P % 16 == 0: row slots start on half-warp boundaries
-    a.T = ((a.c * a.P + 31) / 32) * 32;
+    const int tpr = a.P / (mt == 1 ? Limits<1>::kG : Limits<2>::kG);  // threads per row slot
+    a.c = max(1, budget / tpr);  // P % 16 == 0: row slots start on reduction-group boundaries
+    a.T = ((a.c * tpr + 31) / 32) * 32;
     p.threads = a.T + 32;
     if (p.threads > max_threads || a.P % 16 != 0) {
         p.ok = false;

@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = issued_x - kNX; i < issued_x; ++i)
                 if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
         }
+        __syncwarp();  // lanes 1..31 wait for the producer lane before the cluster barriers
     } else if (warp == 1) {
         // MMA issue: the whole warp waits and loops (converged); one elected
         // lane issues the MMAs and commits
@@ -307,8 +308,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                     rw[4 * i + 2] = q.z;
                     rw[4 * i + 3] = q.w;
                 }
-                __syncwarp();  // every lane holds its part of the stage: release it
-                if (lane == 0) mbar_arrive(&w_empty[wsl]);
                 // A slot (stage, half): 128 k = two 64-k pieces of 32 columns
                 if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[asl], aph ^ 1, abort_flag, err))) return false;
                 tc_fence_after();
@@ -328,7 +327,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();  // every lane's stores are done
-                if (lane == 0) mbar_arrive(&a_full[asl]);
+                if (lane == 0) {
+                    mbar_arrive(&a_full[asl]);
+                    // the weight stage goes back only now that every lane has
+                    // used what it loaded: a release right after the shared
+                    // loads let the next TMA fill of the slot overtake loads
+                    // still in flight (an async-proxy write after generic
+                    // reads), seen as stale rows when weights came from L2
+                    mbar_arrive(&w_empty[wsl]);
+                }
                 if (++wsl == kNW) {
                     wsl = 0;
                     wph ^= 1;

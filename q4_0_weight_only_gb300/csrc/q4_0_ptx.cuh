@@ -319,8 +319,21 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 
 // Cluster-wide barrier (every thread of every CTA of the cluster arrives).
+// The .aligned forms must be executed by whole, converged warps: a warp whose
+// lanes took different roles (one lane issuing copies, the others idle) meets
+// at __syncwarp() first.  Reached by part of a warp, the arrival may count for
+// the whole warp and the late lanes' arrival for the next barrier, which would
+// let a CTA leave while its peers still read its shared memory.
 __device__ __forceinline__ void cluster_sync() {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Named barrier `id` over `nthreads` threads (whole warps), same convergence
+// rule as above.
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.

@@ -136,6 +136,23 @@ def test_deterministic():
         assert torch.equal(y1, y2)
 
 
+def test_batched_cluster_reduction_repeats_bitwise():
+    """Batched decode of the down projection (K = 17408) splits K over 7-CTA
+    clusters and sums the partial tiles through distributed shared memory;
+    with 280 CTAs the last clusters start as earlier ones leave.  Repeats of
+    the same call must agree bit for bit (a CTA leaving before its peers have
+    read its partial tile shows up here as differing outputs)."""
+    q4 = lib()
+    N, K = synth.SHAPES["down"]
+    wd = wq_dev(oracle.get().quantize(synth.decode_weights("down")))
+    for M in (16, 32):
+        xd = x_dev(synth.batched_x("down", M))
+        y0 = q4.matmul(xd, wd, N, K).clone()
+        for _ in range(12):
+            assert torch.equal(q4.matmul(xd, wd, N, K), y0)
+        assert q4.device_error() == 0
+
+
 def test_output_guards_untouched():
     q4 = lib()
     for M, N, K in ((1, 33, 256), (5, 130, 512), (70, 130, 512)):
