@@ -357,22 +357,29 @@ __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
 // Sixteen elements (half `part` of block b of x row m) -> fixed point,
 // written into the pair record; the two threads of a block (consecutive
 // lanes) agree on the block's exponent and sum through a shuffle.  `live` is
-// false for lanes past the end (they still take part in the shuffles).
-__device__ __forceinline__ void convert_part(const uint16_t *__restrict__ xrow, int b, int part,
-                                             bool live, uint32_t *__restrict__ rec) {
-    float xv[16];
+// false for lanes past the end (they still take part in the shuffles).  The
+// two 16-byte loads are issued by load_part, ahead of every conversion of the
+// thread, so that a CTA pays one load round trip for all of x.
+__device__ __forceinline__ void load_part(const uint16_t *__restrict__ xrow, int b, int part, bool live,
+                                          uint4 (&u)[2]) {
     if (live && xrow) {
         const uint4 *src = reinterpret_cast<const uint4 *>(xrow + (int64_t)b * 32) + 2 * part;
-        const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-        const uint32_t w8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            xv[2 * h] = __uint_as_float(w8[h] << 16);
-            xv[2 * h + 1] = __uint_as_float(w8[h] & 0xFFFF0000u);
-        }
+        u[0] = __ldg(src);
+        u[1] = __ldg(src + 1);
     } else {
+        u[0] = make_uint4(0u, 0u, 0u, 0u);
+        u[1] = u[0];
+    }
+}
+
+__device__ __forceinline__ void convert_part(const uint4 (&u)[2], int b, int part, bool live,
+                                             uint32_t *__restrict__ rec) {
+    float xv[16];
+    const uint32_t w8[8] = {u[0].x, u[0].y, u[0].z, u[0].w, u[1].x, u[1].y, u[1].z, u[1].w};
 #pragma unroll
-        for (int j = 0; j < 16; ++j) xv[j] = 0.f;
+    for (int h = 0; h < 8; ++h) {
+        xv[2 * h] = __uint_as_float(w8[h] << 16);
+        xv[2 * h + 1] = __uint_as_float(w8[h] & 0xFFFF0000u);
     }
     float amax = 0.f;
 #pragma unroll
@@ -489,11 +496,19 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
         // converted: a CTA that starts after the previous kernel has ended
         // would otherwise find its x loads queued behind a ring's worth of
         // weight bytes arriving at the same SM, and such a late CTA decides
-        // when the kernel ends.
+        // when the kernel ends.  With one row of x the rest of the ring's
+        // first fill is requested into L2 meanwhile (no shared-memory
+        // destination, so the SM's incoming path stays free for x); it then
+        // arrives from L2 once x is ready.  Prefetching deeper than the ring,
+        // or with two rows of x, measured slower.
         if (lane == 0) {
             constexpr int kPreWait = 3;
             const int pre = min(kPreWait, min(a.S, nst));
             for (int i = 0; i < pre; ++i) issue(i);
+            if (MT == 1)
+                for (int i = pre; i < a.S && i < nst; ++i)
+                    bulk_prefetch_l2(wq + stage_row0(i) * a.rowbytes, (uint32_t)stage_rows(i) * (uint32_t)a.rowbytes,
+                                     policy);
             pdl_wait();
             mbar_wait(xready, 0, abort_flag, err);
             for (int i = pre; i < a.S && i < nst; ++i) issue(i);
@@ -513,14 +528,28 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
     pdl_wait();
     const int nb = 2 * a.P;
     const int nparts = 2 * MT * nb;  // two threads per 32-element block
-    for (int t0 = tid - lane; t0 < nparts; t0 += a.T) {  // warp-uniform trip count
-        const int t = t0 + lane;
-        const bool live = t < nparts;
-        const int q = live ? t : nparts - 1;
-        const int blk_id = q >> 1, part = q & 1;
-        const int m = blk_id / nb, b = blk_id - m * nb;
-        convert_part(m < a.mrows ? x + (int64_t)m * a.K : nullptr, b, part, live,
-                     xsm + ((size_t)m * a.P + (b >> 1)) * kPairWords);
+    constexpr int kParts = 4;  // parts per thread per load round
+    static_assert(MT <= 2, "the row of a block is blk_id >= nb");
+    for (int t0 = tid - lane; t0 < nparts; t0 += kParts * a.T) {  // warp-uniform trip counts
+        uint4 u[kParts][2];
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) {
+            if (t0 + k * a.T < nparts) {
+                const int t = t0 + k * a.T + lane;
+                const int q = t < nparts ? t : nparts - 1;
+                const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0;
+                load_part(m < a.mrows ? x + (int64_t)m * a.K : nullptr, blk_id - m * nb, q & 1, t < nparts, u[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) {
+            if (t0 + k * a.T < nparts) {
+                const int t = t0 + k * a.T + lane;
+                const int q = t < nparts ? t : nparts - 1;
+                const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0, b = blk_id - m * nb;
+                convert_part(u[k], b, q & 1, t < nparts, xsm + ((size_t)m * a.P + (b >> 1)) * kPairWords);
+            }
+        }
     }
     named_bar_sync(1, a.T);
     if (tid == 0) mbar_arrive(xready);

@@ -138,6 +138,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return p;
 }
 
+// Bring `bytes` (a multiple of 16, 16-byte aligned) into L2 without a
+// shared-memory destination.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
 // 1-D bulk copy with an L2 cache policy.
 __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                               uint64_t policy) {
