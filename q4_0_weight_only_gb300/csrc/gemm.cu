@@ -9,8 +9,11 @@
 //     tiles keep the result well inside the error budget (bf16 weight tiles
 //     would not);
 //   * one CTA computes a 128 (weight rows) x TM (x rows) tile of y^T, TM a
-//     multiple of 16 up to 256 chosen per call so that the M tiles carry the
-//     least padding (M = 272 -> two tiles of 144);
+//     multiple of 16 chosen per call: one tile while M <= 320 (every further
+//     tile dequantises each weight tile again; M = 272 is one tile, not two
+//     of 144), else the fewest tiles of at most 256 rows with the least
+//     padding.  Past 256 rows an x stage arrives as two TMA boxes and each
+//     k step takes a second MMA for rows 256.. (an MMA is at most 256 wide);
 //     warp 0 streams Q4_0 weight tiles [128 rows x 256 k] (144 bytes per row)
 //     and 128-byte-swizzled x tiles [TM rows x 64 k] with tensor TMA;
 //   * warps 2-5 (one thread per weight row) unpack nibbles, apply the scale
@@ -40,6 +43,7 @@ constexpr int kKW = 256;                    // k per weight stage
 constexpr int kWRowBytes = kKW / 32 * 18;   // 144
 constexpr int kWStageBytes = kTileN * kWRowBytes;
 constexpr int kNW = 3, kNX = 4, kNA = 4;    // ring depths
+constexpr int kMaxTileRows = 320;            // x rows per tile: 4 x stages of 40 KB + the weight ring fit
 constexpr int kThreads = 192;
 
 __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
@@ -156,6 +160,9 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
     }
 }
 
+// kTall: x tiles of more than 256 rows (two TMA boxes per x stage, a second
+// MMA per k step); a separate instantiation keeps the common path unchanged.
+template <bool kTall>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 float *__restrict__ y, float *__restrict__ part, int M, int N, int K, int TM, int ybf16,
@@ -232,8 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
-                    tma_load_2d(xring + xsl * Cfg.x_stage, &xmap, w_begin * (kKW / kKB) * kKB + s * kKB, m0,
-                                &x_full[xsl]);
+                    const int kx = w_begin * (kKW / kKB) * kKB + s * kKB;
+                    if (!kTall) {
+                        tma_load_2d(xring + xsl * Cfg.x_stage, &xmap, kx, m0, &x_full[xsl]);
+                    } else {  // a TMA box is at most 256 rows: two boxes of TM / 2
+                        tma_load_2d(xring + xsl * Cfg.x_stage, &xmap, kx, m0, &x_full[xsl]);
+                        tma_load_2d(xring + xsl * Cfg.x_stage + (TM / 2) * 128, &xmap, kx, m0 + TM / 2,
+                                    &x_full[xsl]);
+                    }
                     ++issued_x;
                 }
                 if (!ok) break;
@@ -247,7 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // MMA issue: the whole warp waits and loops (converged); one elected
         // lane issues the MMAs and commits
-        const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)TM);
+        // an MMA is at most 256 wide: a taller x tile takes a second MMA per
+        // k step over rows 256.. (D columns 256..), with the same A
+        const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)(kTall ? 256 : TM));
+        const uint32_t idesc2 = idesc_f16_f32(kTileN, (uint32_t)(kTall ? TM - 256 : 16));
         for (int s = 0; s < KS; ++s) {
             const int xsl = s % kNX, asl = s % kNA;
             if (!__all_sync(0xffffffffu, mbar_wait(&x_full[xsl], (s / kNX) & 1, abort_flag, err))) break;
@@ -256,9 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) {
                 const uint64_t bdesc = smem_desc_k128(xring + xsl * Cfg.x_stage);
 #pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk)
+                for (int kk = 0; kk < kKB / 16; ++kk) {
                     mma_f16_ts(d_tmem, a_tmem + asl * 32 + kk * 8, bdesc + 2 * kk, idesc,
                                (s | kk) != 0);
+                    if (kTall)  // rows 256.. start 256 x 128 bytes into the stage
+                        mma_f16_ts(d_tmem + 256, a_tmem + asl * 32 + kk * 8, bdesc + (256 * 128 >> 4) + 2 * kk,
+                                   idesc2, (s | kk) != 0);
+                }
                 mma_commit(&x_empty[xsl]);
                 mma_commit(&a_empty[asl]);
             }
@@ -381,7 +401,7 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, fl
     {
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {kKB, (cuuint32_t)TM};
+        const cuuint32_t box[2] = {kKB, (cuuint32_t)(TM <= 256 ? TM : TM / 2)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x16), dims, strides, box,
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -399,10 +419,12 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, fl
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_kernel), (int)Cfg.smem);
+    const bool tall = TM > 256;
+    auto kernel = tall ? gemm_kernel<true> : gemm_kernel<false>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM), (unsigned)splits);
-    e = launch_pdl(gemm_kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr,
+    e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr,
                    (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
     if (e != cudaSuccess || splits == 1) return e;
     const int64_t n4 = M * N / 4;
@@ -416,8 +438,11 @@ namespace {
 
 int64_t x16_bytes(int64_t M, int64_t K) { return (M * K * 2 + 255) / 256 * 256; }
 
+// Rows of x per CTA tile: one tile up to kMaxTileRows rows (each extra tile
+// dequantises every weight tile once more), else the fewest tiles of at most
+// 256 rows; the smallest multiple of 16 that covers M in that many tiles.
 int tile_rows(int64_t M) {
-    const int64_t tiles_m = (M + 255) / 256;
+    const int64_t tiles_m = M <= kMaxTileRows ? 1 : (M + 255) / 256;
     return (int)(((M + tiles_m - 1) / tiles_m + 15) / 16 * 16);
 }
 
@@ -462,8 +487,6 @@ cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf
     cudaError_t e = launch_pdl(x_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
                                reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(x16), n8);
     if (e != cudaSuccess) return e;
-    // fewest M tiles of at most 256 rows, then the smallest multiple of 16
-    // that covers M in that many tiles
     return launch_tm(tile_rows(M), splits < 1 ? 1 : splits, x16, wq, y, ybf16, part, M, N, K, s, err);
 }
 

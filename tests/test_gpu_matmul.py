@@ -35,7 +35,9 @@ def test_gemv_small(M, N, K):
 
 SMALL_GEMM = [(1, 128, 256), (16, 128, 256), (17, 200, 512), (32, 384, 768), (33, 128, 256),
               (64, 1000, 1280), (65, 129, 2304), (100, 256, 1024), (128, 640, 512),
-              (129, 300, 768), (256, 128, 1024), (300, 520, 1536), (513, 384, 512)]
+              (129, 300, 768), (256, 128, 1024), (300, 520, 1536), (513, 384, 512),
+              # one x tile of more than 256 rows: a second MMA per k step
+              (257, 130, 512), (272, 384, 1024), (320, 256, 2048), (321, 200, 512)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALL_GEMM)
