@@ -9,11 +9,11 @@
 //     tiles keep the result well inside the error budget (bf16 weight tiles
 //     would not);
 //   * one CTA computes a 128 (weight rows) x TM (x rows) tile of y^T, TM a
-//     multiple of 16 chosen per call: one tile while M <= 320 (every further
-//     tile dequantises each weight tile again; M = 272 is one tile, not two
-//     of 144), else the fewest tiles of at most 256 rows with the least
-//     padding.  Past 256 rows an x stage arrives as two TMA boxes and each
-//     k step takes a second MMA for rows 256.. (an MMA is at most 256 wide);
+//     multiple of 16 chosen per call: the fewest tiles of at most 320 rows
+//     (every further tile dequantises each weight tile again; M = 272 is one
+//     tile, not two of 144), with the least padding.  Past 256 rows an x
+//     stage arrives as two TMA boxes and each k step takes a second MMA for
+//     rows 256.. (an MMA is at most 256 wide);
 //     warp 0 streams Q4_0 weight tiles [128 rows x 256 k] (144 bytes per row)
 //     and 128-byte-swizzled x tiles [TM rows x 64 k] with tensor TMA;
 //   * warps 2-5 (one thread per weight row) unpack nibbles, apply the scale
@@ -438,11 +438,11 @@ namespace {
 
 int64_t x16_bytes(int64_t M, int64_t K) { return (M * K * 2 + 255) / 256 * 256; }
 
-// Rows of x per CTA tile: one tile up to kMaxTileRows rows (each extra tile
-// dequantises every weight tile once more), else the fewest tiles of at most
-// 256 rows; the smallest multiple of 16 that covers M in that many tiles.
+// Rows of x per CTA tile: the fewest tiles of at most kMaxTileRows rows
+// (each extra tile dequantises every weight tile once more), then the
+// smallest multiple of 16 that covers M in that many tiles.
 int tile_rows(int64_t M) {
-    const int64_t tiles_m = M <= kMaxTileRows ? 1 : (M + 255) / 256;
+    const int64_t tiles_m = (M + kMaxTileRows - 1) / kMaxTileRows;
     return (int)(((M + tiles_m - 1) / tiles_m + 15) / 16 * 16);
 }
 
