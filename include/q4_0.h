@@ -154,6 +154,30 @@ int q4_0_matmul_ex(const uint16_t *x, const uint8_t *wq, void *y, int y_type,
                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * q4_0_matmul_host -- the dispatcher with x and y in host memory: one call
+ * copies x ([M][K] bf16 row-major, host) into the workspace, runs the matmul
+ * there, and copies y ([M][N] of `y_type`, host) back, all asynchronously on
+ * `stream` in that order.  wq is the device Q4_0 matrix as for q4_0_matmul.
+ * When both host buffers are page-locked memory the device can address
+ * (cudaHostAlloc / cudaHostRegister; on a GB300 the Grace memory is coherent
+ * with the GPU over NVLink-C2C) and 16-byte aligned there, the kernels read
+ * x and write y in host memory directly and no copy is issued; otherwise x
+ * and y are copied with plain cudaMemcpyAsync (page-locked buffers let the
+ * copies overlap the host).  Either way the caller synchronises `stream`
+ * before reading y (or reusing x).
+ * Workspace: device memory, 16-byte aligned, of at least
+ * q4_0_matmul_host_workspace_bytes(M, N, K, y_type) bytes: the device copies
+ * of x and y (each rounded up to 256 bytes) and the matmul's own scratch;
+ * a missing, misaligned or small workspace is Q4_0_ERR_WORKSPACE.
+ * The size query returns 0 for arguments the call would reject.
+ * Returns as q4_0_matmul_ex; a failed copy is Q4_0_ERR_CUDA.
+ */
+size_t q4_0_matmul_host_workspace_bytes(int64_t M, int64_t N, int64_t K, int y_type);
+int q4_0_matmul_host(const uint16_t *x_host, const uint8_t *wq, void *y_host, int y_type,
+                     int64_t M, int64_t N, int64_t K,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * q4_0_gemv -- the decode kernels alone (what q4_0_matmul runs for
  * M <= 32).  Same arguments, layout and result contract as q4_0_matmul;
  * M <= 32 (larger M is UNSUPPORTED).  M <= 2 needs no scratch; for

@@ -37,6 +37,8 @@ SIGNATURES = {
     "q4_0_matmul_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "q4_0_matmul_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_matmul_ex": ([_P, _P, _P, _INT, _I64, _I64, _I64, _P, _SZ, _P], _INT),
+    "q4_0_matmul_host_workspace_bytes": ([_I64, _I64, _I64, _INT], _SZ),
+    "q4_0_matmul_host": ([_P, _P, _P, _INT, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemv": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "q4_0_gemv_workspace_bytes": ([_I64, _I64], _SZ),
     "q4_0_gemv_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
@@ -125,13 +127,32 @@ def quantize(w: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Te
     return out
 
 
+def _q4_bytes(N: int, K: int) -> int:
+    # q4_0_weight_bytes without a library call (it runs on every matmul call)
+    return N * (K // 32) * 18 if N > 0 and K > 0 and K % 32 == 0 else 0
+
+
+_ws_cache = {}
+
+
+def _ws_bytes(fn: str, *args) -> int:
+    # a workspace size depends on the arguments and on the current device
+    # (the GEMM's K split follows its SM count): one library query per
+    # distinct (device, call shape)
+    key = (fn, torch.cuda.current_device()) + args
+    v = _ws_cache.get(key)
+    if v is None:
+        v = _ws_cache[key] = int(getattr(lib(), fn)(*args))
+    return v
+
+
 def _mm_args(x, wq, N, K, out, out_dtype=torch.float32):
     _need(x, "x", torch.bfloat16, 2)
     _need(wq, "wq", torch.uint8, 2)
     M = x.shape[0]
     if x.shape[1] != K:
         raise ValueError("x.shape[1] must equal K")
-    if wq.numel() != weight_bytes(N, K):
+    if wq.numel() != _q4_bytes(N, K):
         raise ValueError("wq does not hold an N x K Q4_0 matrix")
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=x.device)
@@ -159,16 +180,53 @@ def matmul(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor 
         raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
     M, out = _mm_args(x, wq, N, K, out, out_dtype)
     if out_dtype == torch.bfloat16:
-        ws, wsb = _workspace(int(lib().q4_0_matmul_workspace_bytes(M, N, K)), x.device, workspace)
+        ws, wsb = _workspace(_ws_bytes("q4_0_matmul_workspace_bytes", M, N, K), x.device, workspace)
         _check(lib().q4_0_matmul_ex(x.data_ptr(), wq.data_ptr(), out.data_ptr(), Y_BF16, M, N, K,
                                     ws.data_ptr() if ws is not None else None, wsb, _stream(stream)),
                "q4_0_matmul_ex")
         return out
-    ws, wsb = _workspace(int(lib().q4_0_matmul_workspace_bytes(M, N, K)), x.device, workspace)
+    ws, wsb = _workspace(_ws_bytes("q4_0_matmul_workspace_bytes", M, N, K), x.device, workspace)
     _check(lib().q4_0_matmul_ws(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
                                 ws.data_ptr() if ws is not None else None, wsb, _stream(stream)),
            "q4_0_matmul")
     return out
+
+
+def matmul_host(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
+                workspace: torch.Tensor = None, stream=None, out_dtype=torch.float32) -> torch.Tensor:
+    """y = x W^T with x and y in host memory, through q4_0_matmul_host: x bf16
+    [M, K] on the host (page-locked for asynchronous copies), wq Q4_0 on the
+    device, y [M, N] of out_dtype on the host (allocated page-locked when not
+    given).  One call copies x in, runs the dispatcher and copies y back on
+    the stream; synchronise the stream before reading y.  workspace: a device
+    uint8 tensor of at least host_workspace_bytes(M, N, K, out_dtype)."""
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or x.is_cuda or x.dim() != 2 \
+            or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D bf16 host tensor")
+    _need(wq, "wq", torch.uint8, 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] must equal K")
+    if wq.numel() != _q4_bytes(N, K):
+        raise ValueError("wq does not hold an N x K Q4_0 matrix")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, pin_memory=True)
+    if not isinstance(out, torch.Tensor) or out.dtype != out_dtype or out.is_cuda \
+            or tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] host tensor of out_dtype")
+    yt = Y_BF16 if out_dtype == torch.bfloat16 else Y_F32
+    ws, wsb = _workspace(_ws_bytes("q4_0_matmul_host_workspace_bytes", M, N, K, yt), wq.device, workspace)
+    _check(lib().q4_0_matmul_host(x.data_ptr(), wq.data_ptr(), out.data_ptr(), yt, M, N, K,
+                                  ws.data_ptr() if ws is not None else None, wsb, _stream(stream)),
+           "q4_0_matmul_host")
+    return out
+
+
+def host_workspace_bytes(M: int, N: int, K: int, out_dtype=torch.float32) -> int:
+    """Device scratch for matmul_host (q4_0_matmul_host_workspace_bytes)."""
+    return int(lib().q4_0_matmul_host_workspace_bytes(M, N, K, Y_BF16 if out_dtype == torch.bfloat16 else Y_F32))
 
 
 def matmul_alloc(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,

@@ -114,6 +114,17 @@ int check_matmul_args(const void *x, const void *wq, const void *y, int64_t M, i
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? Q4_0_OK : Q4_0_ERR_CUDA; }
 
+// The device address of page-locked host memory the current device can
+// access, or nullptr (pageable or unknown memory, or a query error).
+const void *host_mapping(const void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -283,6 +294,52 @@ int q4_0_matmul_ex(const uint16_t *x, const uint8_t *wq, void *y, int y_type, in
     if (!workspace && workspace_bytes == 0 && q4_0_matmul_workspace_bytes(M, N, K) != 0)
         return matmul_alloc_impl(x, wq, yf, bf16, M, N, K, stream);
     return matmul_ws_impl(x, wq, yf, bf16, M, N, K, workspace, workspace_bytes, stream);
+}
+
+size_t q4_0_matmul_host_workspace_bytes(int64_t M, int64_t N, int64_t K, int y_type) {
+    if (y_type != Q4_0_Y_F32 && y_type != Q4_0_Y_BF16) return 0;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return 0;
+    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 24) || M * K > (1ll << 40) || M * N > (1ll << 40))
+        return 0;
+    const size_t ysz = y_type == Q4_0_Y_BF16 ? 2 : 4;
+    const size_t xb = ((size_t)M * (size_t)K * 2 + 255) / 256 * 256;
+    const size_t yb = ((size_t)M * (size_t)N * ysz + 255) / 256 * 256;
+    return xb + yb + q4_0_matmul_workspace_bytes(M, N, K);
+}
+
+int q4_0_matmul_host(const uint16_t *x_host, const uint8_t *wq, void *y_host, int y_type, int64_t M, int64_t N,
+                     int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
+    if (y_type != Q4_0_Y_F32 && y_type != Q4_0_Y_BF16) return Q4_0_ERR_INVALID_ARG;
+    if (!x_host || !wq || !y_host) return Q4_0_ERR_INVALID_ARG;
+    const size_t need = q4_0_matmul_host_workspace_bytes(M, N, K, y_type);
+    if (need == 0) return Q4_0_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return Q4_0_ERR_WORKSPACE;
+    const bool bf16 = y_type == Q4_0_Y_BF16;
+    const size_t ysz = bf16 ? 2 : 4;
+    const size_t xbytes = (size_t)M * (size_t)K * 2, ybytes = (size_t)M * (size_t)N * ysz;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint16_t *xd = reinterpret_cast<uint16_t *>(ws);
+    uint8_t *yd = ws + (xbytes + 255) / 256 * 256;
+    uint8_t *rest = yd + (ybytes + 255) / 256 * 256;
+    const size_t rest_bytes = workspace_bytes - (size_t)(rest - ws);
+    // Page-locked host memory that the device can address (on a GB300 the
+    // Grace memory is coherent with the GPU over NVLink-C2C): the kernels
+    // read x and write y there directly, so no copy stands between this call
+    // and the previous one on the stream.  Other host memory is copied.
+    const void *xdev = host_mapping(x_host), *ydev = host_mapping(y_host);
+    if (xdev && ydev && aligned16(xdev) && aligned16(ydev)) {
+        const size_t own = q4_0_matmul_workspace_bytes(M, N, K);
+        return matmul_ws_impl(static_cast<const uint16_t *>(xdev), wq, static_cast<float *>(const_cast<void *>(ydev)),
+                              bf16, M, N, K, own ? rest : nullptr, rest_bytes, stream);
+    }
+    int st = check_matmul_args(xd, wq, yd, M, N, K, true);
+    if (st != Q4_0_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(xd, x_host, xbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return Q4_0_ERR_CUDA;
+    st = matmul_ws_impl(xd, wq, reinterpret_cast<float *>(yd), bf16, M, N, K,
+                        q4_0_matmul_workspace_bytes(M, N, K) ? rest : nullptr, rest_bytes, stream);
+    if (st != Q4_0_OK) return st;
+    return from_cuda(cudaMemcpyAsync(y_host, yd, ybytes, cudaMemcpyDeviceToHost, s));
 }
 
 int q4_0_selftest_wait_timeout(int64_t limit_us, void *stream) {

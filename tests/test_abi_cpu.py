@@ -103,3 +103,32 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError):
         _lib.lib()
+
+
+def test_matmul_host_validates_before_any_copy(lib):
+    """q4_0_matmul_host rejects bad arguments before touching the GPU."""
+    p = ctypes.c_void_p(16)
+    # bad output type, null host buffers
+    assert lib.q4_0_matmul_host(p, p, p, 7, 1, 128, 256, p, 1 << 20, None) == -1
+    assert lib.q4_0_matmul_host(None, p, p, 0, 1, 128, 256, p, 1 << 20, None) == -1
+    assert lib.q4_0_matmul_host(p, p, None, 0, 1, 128, 256, p, 1 << 20, None) == -1
+    # K not a multiple of 32
+    assert lib.q4_0_matmul_host(p, p, p, 0, 1, 128, 100, p, 1 << 20, None) == -1
+    # missing, small or misaligned workspace
+    need = lib.q4_0_matmul_host_workspace_bytes(4, 128, 256, 0)
+    assert lib.q4_0_matmul_host(p, p, p, 0, 4, 128, 256, None, 0, None) == -5
+    assert lib.q4_0_matmul_host(p, p, p, 0, 4, 128, 256, p, need - 1, None) == -5
+    assert lib.q4_0_matmul_host(p, p, p, 0, 4, 128, 256, ctypes.c_void_p(24), need, None) == -5
+
+
+def test_matmul_host_workspace_sizes(lib):
+    """Device copies of x and y (each rounded up to 256 bytes), then the
+    dispatcher's own scratch; 0 for arguments the call rejects."""
+    for M, N, K, yt in ((1, 5120, 5120, 0), (16, 300, 2048, 1), (300, 500, 1024, 0), (3, 100, 96, 1)):
+        ysz = 2 if yt else 4
+        x = (M * K * 2 + 255) // 256 * 256
+        y = (M * N * ysz + 255) // 256 * 256
+        assert lib.q4_0_matmul_host_workspace_bytes(M, N, K, yt) == x + y + lib.q4_0_matmul_workspace_bytes(M, N, K)
+    assert lib.q4_0_matmul_host_workspace_bytes(1, 128, 256, 2) == 0
+    assert lib.q4_0_matmul_host_workspace_bytes(0, 128, 256, 0) == 0
+    assert lib.q4_0_matmul_host_workspace_bytes(1, 128, 100, 0) == 0

@@ -317,3 +317,25 @@ def test_chunked_prefill_m272(shape):
     w, x = synth.small_case(500 + synth.SHAPE_ORDER.index(shape), 272, 8, K, act_outlier_frac=0.01)
     y = q4.matmul(x_dev(x), wq_dev(wq), N, K)
     check_sampled(y, x, wq, N, K, seed=272)
+
+
+def test_matmul_host_equals_device_call():
+    """q4_0_matmul_host gives bit for bit what the device-buffer dispatcher
+    gives: with page-locked buffers (read and written by the kernels in
+    place) and with pageable ones (copied in and out)."""
+    q4 = lib()
+    for M, N, K in ((1, 1000, 5120), (2, 300, 1024), (16, 300, 2048), (64, 260, 1024), (300, 200, 512),
+                    (1, 100, 96)):
+        x, wq = case(8400 + M, M, N, K)
+        wd = wq_dev(wq)
+        x_pageable = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16)
+        for pinned in (True, False):
+            xh = x_pageable.pin_memory() if pinned else x_pageable
+            for dt in (torch.float32, torch.bfloat16):
+                ref = q4.matmul(xh.cuda(), wd, N, K, out_dtype=dt).cpu()
+                out = torch.empty((M, N), dtype=dt, pin_memory=pinned)
+                st = torch.cuda.current_stream()
+                y = q4.matmul_host(xh, wd, N, K, out=out, out_dtype=dt, stream=st)
+                st.synchronize()
+                assert not y.is_cuda and y.dtype == dt
+                assert torch.equal(y, ref), (M, N, K, dt, pinned)
