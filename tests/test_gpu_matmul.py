@@ -339,3 +339,58 @@ def test_matmul_host_equals_device_call():
                 st.synchronize()
                 assert not y.is_cuda and y.dtype == dt
                 assert torch.equal(y, ref), (M, N, K, dt, pinned)
+
+
+def test_graph_capture_replays_bitwise():
+    """A decode step captured into a CUDA graph (decode, batched decode and
+    GEMM calls back to back under programmatic dependent launch, each with
+    its own workspace) replays to the same bits as the direct calls."""
+    q4 = lib()
+    calls = []
+    for M, N, K in ((1, 1000, 5120), (2, 300, 1024), (16, 520, 2048), (40, 300, 1024), (272, 260, 1024),
+                    (1, 100, 96)):
+        x, wq = case(8600 + M + N, M, N, K)
+        xd, wd = x_dev(x), wq_dev(wq)
+        ws = torch.empty(max(1, q4.lib().q4_0_matmul_workspace_bytes(M, N, K)), dtype=torch.uint8, device="cuda")
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        calls.append((xd, wd, N, K, ws, y))
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        ref = [q4.matmul(xd, wd, N, K, workspace=ws, stream=st).clone() for xd, wd, N, K, ws, _ in calls]
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for xd, wd, N, K, ws, y in calls:
+                q4.matmul(xd, wd, N, K, out=y, workspace=ws, stream=st)
+        for _ in range(3):
+            for *_, y in calls:
+                y.fill_(float("nan"))
+            g.replay()
+            st.synchronize()
+            for r, (*_, y) in zip(ref, calls):
+                assert torch.equal(y, r)
+    assert q4.device_error() == 0
+
+
+def test_concurrent_streams():
+    """Calls on two streams at once (each with its own workspace and output)
+    give the results of the same calls run alone."""
+    q4 = lib()
+    jobs = []
+    for i, (M, N, K) in enumerate(((1, 3000, 5120), (16, 1500, 2048), (300, 700, 1024))):
+        x, wq = case(8700 + i, M, N, K)
+        xd, wd = x_dev(x), wq_dev(wq)
+        ref = q4.matmul(xd, wd, N, K)
+        jobs.append((xd, wd, N, K, ref))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for rep in range(4):
+        for j, (xd, wd, N, K, ref) in enumerate(jobs):
+            st = streams[(rep + j) % 2]
+            with torch.cuda.stream(st):
+                outs.append((q4.matmul(xd, wd, N, K, stream=st), ref))
+    torch.cuda.synchronize()
+    for y, ref in outs:
+        assert torch.equal(y, ref)
+    assert q4.device_error() == 0
