@@ -20,11 +20,15 @@
 //     two SM quarters more than the others;
 //   * D = 128 x TM fp32 in tensor memory (TM = 16 or 32, padded rows of x are
 //     zero);
-//   * N is tiled by 128 rows; K is split over the CTAs of a thread-block
-//     cluster (up to 8), each streaming its K range once, and the partial
-//     tiles are summed through distributed shared memory in rank order
-//     (deterministic, no atomics, no global scratch).
-// Waits are bounded; every thread reaches both cluster barriers even when a
+//   * N is tiled by 128 rows; when the tiles alone leave SMs idle, K is
+//     split over S CTAs per tile, each streaming its K range once.  They
+//     write their fp32 partial tiles to the workspace and count themselves
+//     in on the tile's counter; the CTA that completes the count sums the S
+//     partials in split order (deterministic; the only atomic is the integer
+//     count) and writes y.  (Thread-block clusters with a distributed-shared-
+//     memory reduction did the same without global scratch, but a grid of
+//     7-CTA clusters took over 10 us to be dispatched onto the SMs.)
+// Waits are bounded; every thread reaches the closing barriers even when a
 // wait gives up.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -47,7 +51,6 @@ constexpr int kWStageBytes = kTileN * kWRowBytes;
 constexpr int kNW = 3, kNA = 3;  // 32 + 3 x 64 TMEM columns <= 256
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * (2 + kDequantWarps);  // 320
-constexpr int kMaxCluster = 8;
 
 __host__ __device__ constexpr uint32_t cols_pow2(uint32_t v) {
     uint32_t p = 32;
@@ -62,10 +65,8 @@ struct Cfg {
     static constexpr int kNX = TM <= 16 ? 4 : 2;                // x ring (two CTAs fit an SM)
     static constexpr uint32_t kDCols = 32;
     static constexpr uint32_t kCols = cols_pow2(kDCols + kNA * (kKB / 2));
-    static constexpr int kPartStride = TM + 1;  // floats per row of the partial tile
     static constexpr size_t kOffW = (size_t)kNX * kXStage;
-    static constexpr size_t kOffPart = kOffW + (size_t)kNW * kWStageBytes;
-    static constexpr size_t kOffBars = kOffPart + (size_t)kTileN * kPartStride * 4;
+    static constexpr size_t kOffBars = kOffW + (size_t)kNW * kWStageBytes;
     static constexpr int kNumBars = 2 * kNW + 2 * kNX + 2 * kNA + 2;
     static constexpr size_t kSmem = 1024 + kOffBars + kNumBars * 8 + 16;
 };
@@ -119,16 +120,20 @@ __device__ __forceinline__ void swap_mid_pairs(uint32_t &a, uint32_t &b) {
     b = hi;
 }
 
-// x (bf16, [M][K]) -> the binary16 B tiles of gemv_tc_kernel: stage u (256 k)
+// x (bf16, [M][K]) -> the binary16 B tiles of gemv_tc_kernel, and zeroed
+// split-K tile counters for it: stage u (256 k)
 // is four atoms [TM rows x 64 k]; in an atom, row m is 128 bytes whose
 // 16-byte chunk c sits at position c ^ (m & 7) (the 128-byte swizzle named in
 // the MMA's shared-memory descriptor), values in the k order of the weight
 // tiles; rows m >= M are zero.  One thread per 16-byte chunk.
 template <int TM>
 __global__ void __launch_bounds__(256) x_tiles_kernel(const uint16_t *__restrict__ x, uint4 *__restrict__ xt,
-                                                      int M, int K) {
+                                                      int M, int K, unsigned int *__restrict__ tile_cnt,
+                                                      int ncnt) {
     pdl_launch_dependents();
-    pdl_wait();  // x may come from the previous kernel
+    pdl_wait();  // x may come from the previous kernel (and the last one has read its counters)
+    if (blockIdx.x == 0)  // the split-K tile counters of the matmul kernel that follows
+        for (int i = threadIdx.x; i < ncnt; i += blockDim.x) tile_cnt[i] = 0u;
     const int kc8 = K / 8;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)TM * kc8) return;
@@ -152,7 +157,8 @@ __global__ void __launch_bounds__(256) x_tiles_kernel(const uint16_t *__restrict
 template <int TM>
 __global__ void __launch_bounds__(kThreads, 2)
     gemv_tc_kernel(const uint4 *__restrict__ xt, const __grid_constant__ CUtensorMap wmap,
-                   float *__restrict__ y, int M, int N, int K, int ybf16, unsigned int *err) {
+                   float *__restrict__ y, float *__restrict__ part, unsigned int *__restrict__ tile_cnt,
+                   int M, int N, int K, int ybf16, unsigned int *err) {
     using C = Cfg<TM>;
     constexpr int kNX = C::kNX;
     extern __shared__ uint8_t smem_raw[];
@@ -160,7 +166,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *xring = smem;
     uint8_t *wring = smem + C::kOffW;
-    float *part = reinterpret_cast<float *>(smem + C::kOffPart);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);
     uint64_t *w_full = bars, *w_empty = bars + kNW;
     uint64_t *x_full = bars + 2 * kNW, *x_empty = x_full + kNX;
@@ -170,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = gridDim.x;                 // CTAs of the cluster, along K
-    const int rank = (int)cluster_rank();
+    const int S = gridDim.x;                 // CTAs per tile, along K
+    const int rank = blockIdx.x;
     const int n0 = blockIdx.y * kTileN;
     const int KU = K / kKW;
     const int u0 = rank * KU / S, u1 = (rank + 1) * KU / S;
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = issued_x - kNX; i < issued_x; ++i)
                 if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
         }
-        __syncwarp();  // lanes 1..31 wait for the producer lane before the cluster barriers
+        __syncwarp();  // lanes 1..31 wait for the producer lane before the closing barriers
     } else if (warp == 1) {
         // MMA issue: the whole warp waits and loops (converged); one elected
         // lane issues the MMAs and commits
@@ -356,41 +361,50 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (ok) {
                 tc_fence_after();
                 uint32_t v[16];
+                const int n = n0 + r;
+                // one K split: y directly; else this split's partial tile,
+                // [tile][split][m][128 rows] (coalesced over the rows)
+                float *pt = part + ((size_t)blockIdx.y * S + rank) * TM * kTileN + r;
 #pragma unroll
                 for (int c = 0; c < TM; c += 16) {
                     tmem_ld16(d_tmem + lane_base + c, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) part[r * C::kPartStride + c + j] = __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = c + j;
+                        if (m >= M) break;
+                        if (S == 1) {
+                            if (n < N) store_y(y, (int64_t)m * N + n, __uint_as_float(v[j]), ybf16 != 0);
+                        } else {
+                            pt[(size_t)m * kTileN] = __uint_as_float(v[j]);
+                        }
+                    }
                 }
+                if (S > 1) __threadfence();  // the partials before the count below
             }
         }
     }
 
-    // cluster reduction: CTA `rank` sums rows [rank * rpc, ...) of the S
-    // partial tiles in rank order and writes y
-    cluster_sync();
-    {
-        const int rpc = (kTileN + S - 1) / S;
-        const int rb = rank * rpc, re = min(kTileN, rb + rpc);
-        const int nr = max(0, re - rb);
-        for (int e = threadIdx.x; e < nr * TM; e += kThreads) {
-            const int m = e / nr, row = rb + (e - m * nr);
-            const int n = n0 + row;
-            if (m < M && n < N) {
-                float v[kMaxCluster];
-#pragma unroll
-                for (int q = 0; q < kMaxCluster; ++q)
-                    v[q] = q < S ? ld_shared_cluster_f32(map_shared_rank(part + row * C::kPartStride + m, (uint32_t)q))
-                                 : 0.f;
+    // split-K: count this CTA in; the CTA that completes the tile's count
+    // sums the S partial tiles in split order and writes y
+    __shared__ int last_s;
+    __syncthreads();
+    if (S > 1) {
+        if (threadIdx.x == 0) last_s = atomicAdd(&tile_cnt[blockIdx.y], 1u) == (unsigned)(S - 1);
+        __syncthreads();
+        if (last_s) {
+            __threadfence();
+            const float *pt = part + (size_t)blockIdx.y * S * TM * kTileN;
+            for (int e = threadIdx.x; e < M * kTileN; e += kThreads) {
+                const int m = e / kTileN, row = e - m * kTileN;
+                const int n = n0 + row;
+                if (n >= N) continue;
                 float sum = 0.f;
-#pragma unroll
-                for (int q = 0; q < kMaxCluster; ++q) sum += v[q];  // rank order
+                for (int q = 0; q < S; ++q) sum += __ldcg(pt + ((size_t)q * TM + m) * kTileN + row);
                 store_y(y, (int64_t)m * N + n, sum, ybf16 != 0);
             }
         }
     }
-    cluster_sync();
     if (warp == 1) {
         if (lane == 0) {
             mma_commit(drain);
@@ -421,9 +435,22 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// Workspace: the x tiles, then room for 2 * SMs partial tiles (S * tiles
+// never exceeds that when S > 1), then 2 * SMs tile counters.
+struct WorkspaceLayout {
+    size_t part_off, cnt_off, bytes;
+    WorkspaceLayout(int tm, int64_t K, int sms) {
+        const size_t xt = (size_t)tm * (size_t)K * 2;
+        part_off = (xt + 255) / 256 * 256;
+        const size_t pb = (size_t)2 * (size_t)sms * kTileN * (size_t)tm * 4;
+        cnt_off = part_off + pb;
+        bytes = cnt_off + ((size_t)2 * (size_t)sms * 4 + 255) / 256 * 256 * (sms > 0 ? 1 : 0);
+    }
+};
+
 template <int TM>
 cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
-                      int64_t K, void *xtiles, cudaStream_t s, unsigned int *err) {
+                      int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
     using C = Cfg<TM>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -447,31 +474,38 @@ cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16
     const int sms = device_sm_count(dev);
     const int64_t tiles = (N + kTileN - 1) / kTileN;
     const int64_t KU = K / kKW;
-    // split K so that about two CTAs per SM are busy, at most 8 per cluster
+    // split K so that about two CTAs per SM are busy: S * tiles <= 2 * SMs,
+    // which bounds the partial tiles the workspace holds
     int64_t S = tiles > 0 ? (2 * (int64_t)sms) / tiles : 1;
-    S = S < 1 ? 1 : (S > kMaxCluster ? kMaxCluster : S);
+    S = S < 1 ? 1 : S;
     if (S > KU) S = KU;
-    if (tiles > 65535) return cudaErrorInvalidValue;
+    if (tiles > 65535 || S > 65535) return cudaErrorInvalidValue;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const WorkspaceLayout L(TM, K, sms);
+    float *part = reinterpret_cast<float *>(ws + L.part_off);
+    unsigned int *cnt = reinterpret_cast<unsigned int *>(ws + L.cnt_off);
     const int64_t chunks = (int64_t)TM * (K / 8);
     e = launch_pdl(x_tiles_kernel<TM>, dim3((unsigned)((chunks + 255) / 256)), dim3(256), 0, s, x,
-                   static_cast<uint4 *>(xtiles), (int)M, (int)K);
+                   reinterpret_cast<uint4 *>(ws), (int)M, (int)K, cnt, S > 1 ? (int)tiles : 0);
     if (e != cudaSuccess) return e;
-    return launch_pdl_cluster(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads),
-                              C::kSmem, s, (unsigned)S, static_cast<const uint4 *>(xtiles), wmap, y, (int)M,
-                              (int)N, (int)K, ybf16 ? 1 : 0, err);
+    return launch_pdl(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads), C::kSmem, s,
+                      reinterpret_cast<const uint4 *>(ws), wmap, y, part, cnt, (int)M, (int)N, (int)K,
+                      ybf16 ? 1 : 0, err);
 }
 
 }  // namespace
 
 size_t gemv_tc_workspace_bytes(int64_t M, int64_t K) {
-    const int64_t tm = M <= 16 ? 16 : 32;
-    return (size_t)(tm * K * 2);
+    int dev = 0;
+    const int sms = cudaGetDevice(&dev) == cudaSuccess ? device_sm_count(dev) : 0;
+    if (sms <= 0) (void)cudaGetLastError();
+    return WorkspaceLayout(M <= 16 ? 16 : 32, K, sms > 0 ? sms : 0).bytes;
 }
 
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
-                           int64_t K, void *xtiles, cudaStream_t s, unsigned int *err) {
-    if (M <= 16) return launch_tm<16>(x, wq, y, ybf16, M, N, K, xtiles, s, err);
-    return launch_tm<32>(x, wq, y, ybf16, M, N, K, xtiles, s, err);
+                           int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
+    if (M <= 16) return launch_tm<16>(x, wq, y, ybf16, M, N, K, workspace, s, err);
+    return launch_tm<32>(x, wq, y, ybf16, M, N, K, workspace, s, err);
 }
 
 }  // namespace q4_0
