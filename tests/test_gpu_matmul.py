@@ -138,12 +138,13 @@ def test_deterministic():
         assert torch.equal(y1, y2)
 
 
-def test_batched_cluster_reduction_repeats_bitwise():
-    """Batched decode of the down projection (K = 17408) splits K over 7-CTA
-    clusters and sums the partial tiles through distributed shared memory;
-    with 280 CTAs the last clusters start as earlier ones leave.  Repeats of
-    the same call must agree bit for bit (a CTA leaving before its peers have
-    read its partial tile shows up here as differing outputs)."""
+def test_batched_split_k_repeats_bitwise():
+    """Batched decode of the down projection (K = 17408) splits K seven ways
+    per 128-row tile: the splits write partial tiles to the workspace and the
+    last one to count in sums them in split order.  Repeats of the same call
+    must agree bit for bit: a partial read before it is complete, a stale
+    weight stage or a counter left over from the previous call shows up here
+    as differing outputs."""
     q4 = lib()
     N, K = synth.SHAPES["down"]
     wd = wq_dev(oracle.get().quantize(synth.decode_weights("down")))
