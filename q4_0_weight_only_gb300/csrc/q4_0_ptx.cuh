@@ -317,43 +317,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ------------------------------------------------------------- clusters
+// ------------------------------------------------------------- barriers
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Cluster-wide barrier (every thread of every CTA of the cluster arrives).
-// The .aligned forms must be executed by whole, converged warps: a warp whose
-// lanes took different roles (one lane issuing copies, the others idle) meets
-// at __syncwarp() first.  Reached by part of a warp, the arrival may count for
-// the whole warp and the late lanes' arrival for the next barrier, which would
-// let a CTA leave while its peers still read its shared memory.
-__device__ __forceinline__ void cluster_sync() {
-    __syncwarp();
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Named barrier `id` over `nthreads` threads (whole warps), same convergence
-// rule as above.
+// Named barrier `id` over `nthreads` threads (whole warps).  The .aligned
+// form must be executed by whole, converged warps: a warp whose lanes took
+// different roles meets at __syncwarp() first.  Reached by part of a warp,
+// the arrival may count for the whole warp and the late lanes' arrival for
+// the next barrier.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_shared_rank(const void *p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
