@@ -399,8 +399,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int m = e / kTileN, row = e - m * kTileN;
                 const int n = n0 + row;
                 if (n >= N) continue;
+                // up to eight partials loaded at once (one L2 round trip),
+                // summed in split order
+                const float *pq = pt + (size_t)m * kTileN + row;
                 float sum = 0.f;
-                for (int q = 0; q < S; ++q) sum += __ldcg(pt + ((size_t)q * TM + m) * kTileN + row);
+                for (int q0 = 0; q0 < S; q0 += 8) {
+                    float v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = q0 + q < S ? __ldcg(pq + (size_t)(q0 + q) * TM * kTileN) : 0.f;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) sum += v[q];
+                }
                 store_y(y, (int64_t)m * N + n, sum, ybf16 != 0);
             }
         }
