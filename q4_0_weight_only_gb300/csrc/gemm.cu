@@ -42,8 +42,12 @@ constexpr int kKB = 64;                     // k per MMA stage
 constexpr int kKW = 256;                    // k per weight stage
 constexpr int kWRowBytes = kKW / 32 * 18;   // 144
 constexpr int kWStageBytes = kTileN * kWRowBytes;
-constexpr int kNW = 3, kNX = 4, kNA = 4;    // ring depths
-constexpr int kMaxTileRows = 320;            // x rows per tile: 4 x stages of 40 KB + the weight ring fit
+constexpr int kNW = 3, kNA = 4;              // weight and A-slot ring depths
+// x ring depth: five stages for tiles of up to 256 rows (an x stage is
+// 32 KB there, and L2 latency under the stream needs the depth); a tall tile
+// (up to kMaxTileRows rows, 40 KB a stage) fits four
+constexpr int kNXShort = 5, kNXTall = 4;
+constexpr int kMaxTileRows = 320;
 constexpr int kThreads = 192;
 
 __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
@@ -56,14 +60,15 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
 struct GemmLayout {
     uint32_t x_stage, d_cols, cols;
     size_t bar_off, smem;
-    __host__ __device__ explicit GemmLayout(int tm) {
+    int num_bars;
+    __host__ __device__ GemmLayout(int tm, int nx) {
         x_stage = (uint32_t)tm * 128;
         d_cols = tm < 32 ? 32 : (uint32_t)((tm + 31) / 32 * 32);
         cols = pow2_at_least(d_cols + kNA * 32);
-        bar_off = (size_t)kNX * x_stage + (size_t)kNW * kWStageBytes;
-        smem = 1024 + bar_off + kNumBars * 8 + 16;
+        bar_off = (size_t)nx * x_stage + (size_t)kNW * kWStageBytes;
+        num_bars = 2 * kNW + 2 * nx + 2 * kNA + 2;
+        smem = 1024 + bar_off + num_bars * 8 + 16;
     }
-    static constexpr int kNumBars = 2 * kNW + 2 * kNX + 2 * kNA + 2;
 };
 
 __device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
@@ -167,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 float *__restrict__ y, float *__restrict__ part, int M, int N, int K, int TM, int ybf16,
                 unsigned int *err) {
-    const GemmLayout Cfg(TM);
+    constexpr int kNX = kTall ? kNXTall : kNXShort;
+    const GemmLayout Cfg(TM, kNX);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *x_full = bars + 2 * kNW, *x_empty = x_full + kNX;
     uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNA;
     uint64_t *d_full = a_empty + kNA, *drain = d_full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + GemmLayout::kNumBars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg.num_bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -394,7 +400,7 @@ EncodeTiledFn encode_fn() {
 
 cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, float *y, bool ybf16, float *part,
                       int64_t M, int64_t N, int64_t K, cudaStream_t s, unsigned int *err) {
-    const GemmLayout Cfg(TM);
+    const GemmLayout Cfg(TM, TM > 256 ? kNXTall : kNXShort);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap xmap, wmap;
@@ -438,11 +444,14 @@ namespace {
 
 int64_t x16_bytes(int64_t M, int64_t K) { return (M * K * 2 + 255) / 256 * 256; }
 
-// Rows of x per CTA tile: the fewest tiles of at most kMaxTileRows rows
-// (each extra tile dequantises every weight tile once more), then the
-// smallest multiple of 16 that covers M in that many tiles.
+// Rows of x per CTA tile.  Each extra tile dequantises every weight tile
+// once more, but tiles of more than 256 rows run with a shallower x ring:
+// they are used when they need at most three quarters as many tiles as
+// 256-row ones (M = 272: one tile instead of two; M = 2048 stays at eight
+// of 256).  Then the smallest multiple of 16 that covers M in that many.
 int tile_rows(int64_t M) {
-    const int64_t tiles_m = (M + kMaxTileRows - 1) / kMaxTileRows;
+    const int64_t t256 = (M + 255) / 256, tall = (M + kMaxTileRows - 1) / kMaxTileRows;
+    const int64_t tiles_m = 4 * tall <= 3 * t256 ? tall : t256;
     return (int)(((M + tiles_m - 1) / tiles_m + 15) / 16 * 16);
 }
 
