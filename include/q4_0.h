@@ -114,8 +114,11 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
 int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y,
                 int64_t M, int64_t N, int64_t K, void *stream);
 
-/* Scratch bytes q4_0_matmul needs for these sizes (0 for M <= 2 when
- * K % 256 == 0; for other K it includes the zero-padded copies of W and x). */
+/* Scratch bytes q4_0_matmul needs for these sizes on the current device
+ * (0 for M <= 2 when K % 256 == 0; for other K it includes the zero-padded
+ * copies of W and x).  The batched-decode and GEMM parts depend on the
+ * device's SM count (room for split-K partial tiles), so query on the device
+ * that will run the call. */
 size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -181,14 +184,17 @@ int q4_0_matmul_host(const uint16_t *x_host, const uint8_t *wq, void *y_host, in
  * q4_0_gemv -- the decode kernels alone (what q4_0_matmul runs for
  * M <= 32).  Same arguments, layout and result contract as q4_0_matmul;
  * M <= 32 (larger M is UNSUPPORTED).  M <= 2 needs no scratch; for
- * 3 <= M <= 32 x is first rounded to binary16 tensor-core tiles in
+ * 3 <= M <= 32 x is first rounded to binary16 tensor-core tiles, and when K
+ * is split across CTAs their partial tiles and counters sit beside them:
  * q4_0_gemv_workspace_bytes(M, K) bytes of scratch, which this entry point
  * takes with cudaMallocAsync / cudaFreeAsync on `stream`.
  */
 int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y,
               int64_t M, int64_t N, int64_t K, void *stream);
 
-/* Scratch bytes of the decode kernels (0 for M <= 2 or M > 32). */
+/* Scratch bytes of the decode kernels on the current device (0 for M <= 2
+ * or M > 32): the binary16 x tiles plus room for two split-K partial tiles
+ * (and counters) per SM, whatever N is. */
 size_t q4_0_gemv_workspace_bytes(int64_t M, int64_t K);
 
 /*
