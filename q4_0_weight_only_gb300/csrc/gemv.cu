@@ -303,11 +303,11 @@ constexpr size_t kSmemLimit = 227 * 1024;
 // rounding beyond fp32 accumulation is X's fixed point for elements far below
 // their block's maximum.
 //
-// Thread (rs, pc) owns block pair pc (64 weights) of every c-th row: its x
-// bytes stay in registers for the whole kernel.  A producer warp streams
-// stages of R whole rows (contiguous bytes) with one bulk TMA copy each; a
-// row's 2P pair partials are reduced by 16-lane butterflies into P/16
-// half-warp partials, summed in order at the end.
+// Thread (rs, tc) owns G block pairs (64 weights each) of every c-th row:
+// their x bytes stay in registers for the whole kernel.  A producer warp
+// streams stages of R whole rows (contiguous bytes) with one bulk TMA copy
+// each; a row's pair partials are reduced by 16/G-lane butterflies into P/16
+// partials, summed in order at the end.
 // ---------------------------------------------------------------------------
 namespace dp {
 
