@@ -394,23 +394,49 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
         if (last_s) {
             __threadfence();
-            const float *pt = part + (size_t)blockIdx.y * S * TM * kTileN;
-            for (int e = threadIdx.x; e < M * kTileN; e += kThreads) {
-                const int m = e / kTileN, row = e - m * kTileN;
-                const int n = n0 + row;
-                if (n >= N) continue;
-                // up to eight partials loaded at once (one L2 round trip),
-                // summed in split order
-                const float *pq = pt + (size_t)m * kTileN + row;
-                float sum = 0.f;
+            // a thread sums groups of four rows of one x row (16-byte loads);
+            // the partials of its two groups and of up to eight splits are
+            // all in flight at once, so the sum costs one L2 round trip per
+            // eight splits rather than one per element.  Each value is still
+            // added in split order.
+            const float4 *pt = reinterpret_cast<const float4 *>(part + (size_t)blockIdx.y * S * TM * kTileN);
+            constexpr int kGroupsPerRow = kTileN / 4;
+            constexpr size_t kSplitStride = (size_t)TM * kGroupsPerRow;  // float4s per partial tile
+            const int groups = M * kGroupsPerRow;
+            for (int g0 = threadIdx.x; g0 < groups; g0 += 2 * kThreads) {
+                float4 sum[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) sum[h] = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int q0 = 0; q0 < S; q0 += 8) {
-                    float v[8];
+                    float4 v[2][8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) v[q] = q0 + q < S ? __ldcg(pq + (size_t)(q0 + q) * TM * kTileN) : 0.f;
+                    for (int h = 0; h < 2; ++h) {
+                        const int g = g0 + h * kThreads;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) sum += v[q];
+                        for (int q = 0; q < 8; ++q)
+                            v[h][q] = g < groups && q0 + q < S ? __ldcg(pt + (size_t)(q0 + q) * kSplitStride + g)
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            sum[h].x += v[h][q].x;
+                            sum[h].y += v[h][q].y;
+                            sum[h].z += v[h][q].z;
+                            sum[h].w += v[h][q].w;
+                        }
                 }
-                store_y(y, (int64_t)m * N + n, sum, ybf16 != 0);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int g = g0 + h * kThreads;
+                    if (g >= groups) continue;
+                    const int m = g / kGroupsPerRow, n = n0 + 4 * (g - m * kGroupsPerRow);
+                    const float s4[4] = {sum[h].x, sum[h].y, sum[h].z, sum[h].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (n + j < N) store_y(y, (int64_t)m * N + n + j, s4[j], ybf16 != 0);
+                }
             }
         }
     }
