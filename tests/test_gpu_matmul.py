@@ -156,6 +156,33 @@ def test_batched_split_k_repeats_bitwise():
         assert q4.device_error() == 0
 
 
+def test_batched_split_k_any_workspace_contents():
+    """The split-K tile counters live in caller scratch that is never
+    cleared: a counter carries the token of the launch that claimed it, and
+    anything else counts as zero.  Workspaces filled with zeros, all-ones or
+    random bytes give the same result bit for bit, and so does a workspace
+    reused after calls of other shapes."""
+    q4 = lib()
+    N, K = synth.SHAPES["o"]
+    wd = wq_dev(oracle.get().quantize(synth.decode_weights("o")))
+    for M in (4, 16, 32):
+        xd = x_dev(synth.batched_x("o", M))
+        nbytes = int(q4.lib().q4_0_matmul_workspace_bytes(M, N, K))
+        ref = q4.matmul(xd, wd, N, K, workspace=torch.zeros(nbytes, dtype=torch.uint8, device="cuda")).clone()
+        g = torch.Generator(device="cuda").manual_seed(M)
+        fills = (torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda"),
+                 torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda", generator=g))
+        for ws in fills:
+            assert torch.equal(q4.matmul(xd, wd, N, K, workspace=ws), ref)
+            assert torch.equal(q4.matmul(xd, wd, N, K, workspace=ws), ref)
+        # the same scratch through calls of other shapes in between
+        ws = fills[1]
+        x2, w2 = case(8100 + M, M, 700, 2048)
+        q4.matmul(x_dev(x2), wq_dev(w2), 700, 2048, workspace=ws)
+        assert torch.equal(q4.matmul(xd, wd, N, K, workspace=ws), ref)
+        assert q4.device_error() == 0
+
+
 def test_output_guards_untouched():
     q4 = lib()
     for M, N, K in ((1, 33, 256), (5, 130, 512), (70, 130, 512)):
