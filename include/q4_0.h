@@ -97,26 +97,33 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
  *         K % 256 == 0 and return UNSUPPORTED otherwise.
  * y[m][n] = sum_k d(n,k) * (q(n,k) - 8) * x[m][k], accumulated in fp32.
  * Dispatch: M <= 2 runs the decode GEMV on CUDA cores (exact integer dot
- * products per 32-weight block on 15-bit fixed-point x, fp32 across blocks);
- * 3 <= M <= 32 runs the batched decode on the tensor cores; M > 32 runs the
- * tcgen05 GEMM (weights dequantised to binary16 tiles, x rounded to
- * binary16, fp32 accumulation in tensor memory).  All meet: per element
+ * products per 32-weight block on 15-bit fixed-point x, fp32 across blocks;
+ * a matrix whose per-row partial sums outgrow one launch's shared memory
+ * runs as several launches over row ranges); 3 <= M <= 32, and M <= 2 with
+ * K > 65536 (x no longer fits shared memory), run the batched decode on the
+ * tensor cores; M > 32 runs the tcgen05 GEMM (weights dequantised to
+ * binary16 tiles, x rounded to binary16, fp32 accumulation in tensor
+ * memory).  All meet: per element
  * |y - y_exact| <= 1e-2 * sum_k |w x| and relative L2 error <= 2e-3.
  * Activations must be finite with |x| <= 65504 (the tensor-core paths round
  * x to binary16).
- * Scratch: the batched-decode (3 <= M <= 32) and GEMM (M > 32) paths need
+ * Scratch: the tensor-core decode and GEMM (M > 32) paths need
  * q4_0_matmul_workspace_bytes(M, N, K) bytes; this entry point takes them
  * with cudaMallocAsync on `stream` and frees them with cudaFreeAsync on the
  * same stream.  Use q4_0_matmul_ws to supply the workspace yourself.
  * Alignment: x, wq and y 16 bytes.
+ * Sizes this build runs (else UNSUPPORTED): M, N <= 2^30, K <= 2^24, each of
+ * M*K, N*K, M*N <= 2^40; on the tensor-core decode N <= 65535 * 128 (its
+ * weight tiles are a grid dimension); on the GEMM at most 65535 x tiles
+ * (M up to about 16.7 million rows).
  * Returns Q4_0_OK, Q4_0_ERR_INVALID_ARG, Q4_0_ERR_UNSUPPORTED or Q4_0_ERR_CUDA.
  */
 int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y,
                 int64_t M, int64_t N, int64_t K, void *stream);
 
 /* Scratch bytes q4_0_matmul needs for these sizes on the current device
- * (0 for M <= 2 when K % 256 == 0; for other K it includes the zero-padded
- * copies of W and x).  The batched-decode and GEMM parts depend on the
+ * (0 for M <= 2 when K % 256 == 0 and K <= 65536; for other K it includes
+ * the zero-padded copies of W and x).  The batched-decode and GEMM parts depend on the
  * device's SM count (room for split-K partial tiles), so query on the device
  * that will run the call. */
 size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K);
@@ -183,18 +190,19 @@ int q4_0_matmul_host(const uint16_t *x_host, const uint8_t *wq, void *y_host, in
 /*
  * q4_0_gemv -- the decode kernels alone (what q4_0_matmul runs for
  * M <= 32).  Same arguments, layout and result contract as q4_0_matmul;
- * M <= 32 (larger M is UNSUPPORTED).  M <= 2 needs no scratch; for
- * 3 <= M <= 32 x is first rounded to binary16 tensor-core tiles, and when K
- * is split across CTAs their partial tiles and counters sit beside them:
+ * M <= 32 (larger M is UNSUPPORTED).  M <= 2 with K <= 65536 needs no
+ * scratch; on the tensor-core decode (3 <= M <= 32, or larger K) x is first
+ * rounded to binary16 tensor-core tiles, and when K is split across CTAs
+ * their partial tiles and counters sit beside them:
  * q4_0_gemv_workspace_bytes(M, K) bytes of scratch, which this entry point
  * takes with cudaMallocAsync / cudaFreeAsync on `stream`.
  */
 int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y,
               int64_t M, int64_t N, int64_t K, void *stream);
 
-/* Scratch bytes of the decode kernels on the current device (0 for M <= 2
- * or M > 32): the binary16 x tiles plus room for two split-K partial tiles
- * (and counters) per SM, whatever N is. */
+/* Scratch bytes of the decode kernels on the current device (0 for M > 32,
+ * and for M <= 2 with K <= 65536): the binary16 x tiles plus room for two
+ * split-K partial tiles (and counters) per SM, whatever N is. */
 size_t q4_0_gemv_workspace_bytes(int64_t M, int64_t K);
 
 /*

@@ -191,7 +191,7 @@ int gemv_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int
                  void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
-    if (M > 32) return Q4_0_ERR_UNSUPPORTED;
+    if (M > 32 || !gemv_shape_supported(M, N, K)) return Q4_0_ERR_UNSUPPORTED;
     const size_t need = gemv_workspace_bytes(M, K);
     if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return Q4_0_ERR_WORKSPACE;
@@ -205,6 +205,7 @@ int gemm_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_
               void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
+    if (!gemm_shape_supported(M, N, K)) return Q4_0_ERR_UNSUPPORTED;
     // split K only if the workspace has room for the partial tiles
     int splits = current_splits(M, N, K);
     if (workspace_bytes < gemm_workspace_bytes(M, N, K, splits)) splits = 1;
@@ -221,6 +222,8 @@ int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, i
                    void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K, true);
     if (st != Q4_0_OK) return st;
+    const int64_t kk = K % 256 != 0 ? padded_k(K) : K;
+    if (M <= 32 ? !gemv_shape_supported(M, N, kk) : !gemm_shape_supported(M, N, kk)) return Q4_0_ERR_UNSUPPORTED;
     if (K % 256 != 0) {
         // copy W and x, zero-padded to a multiple of 256, then run the padded problem
         const size_t pad = pad_bytes(M, N, K);

@@ -480,6 +480,15 @@ int gemm_splits(int64_t M, int64_t N, int64_t K, int sms) {
     return best;
 }
 
+// The launch grids: M tiles in gridDim.y (at most 65535), N tiles in
+// gridDim.x, and the x pre-pass at one thread per eight elements.
+bool gemm_shape_supported(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 1) return false;
+    const int tm = tile_rows(M);
+    return (M + tm - 1) / tm <= 65535 && (N + kTileN - 1) / kTileN <= 0x7FFFFFFF &&
+           (M * K / 8 + 255) / 256 <= 0x7FFFFFFF;
+}
+
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {
     size_t b = (size_t)x16_bytes(M, K);
     if (splits > 1) b += (size_t)splits * (size_t)M * (size_t)N * 4;
@@ -492,7 +501,7 @@ cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf
     float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + x16_bytes(M, K));
     const int64_t n8 = M * K / 8;
     const int64_t blocks = (n8 + 255) / 256;
-    if (blocks > 0x7FFFFFFF || (M + 15) / 16 > 65535) return cudaErrorInvalidValue;
+    if (!gemm_shape_supported(M, N, K)) return cudaErrorInvalidValue;
     cudaError_t e = launch_pdl(x_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
                                reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(x16), n8);
     if (e != cudaSuccess) return e;

@@ -41,6 +41,7 @@ constexpr int kSlotBytes = 2 * kRowChunkBytes;            // two rows: 1152
 
 struct GemvArgs {
     int64_t N, K;
+    int64_t ldy;   // row stride of y (the full N when N is covered by several launches)
     int P;         // block pairs per row (K / 64)
     int C;         // chunks per row
     int nb;        // blocks per row (K / 32)
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = t / nrows, r = t - m * nrows;
         float s = 0.f;
         for (int c = 0; c < C; ++c) s += part[(r * C + c) * MT + m];
-        store_y(y, (int64_t)m * a.N + r0 + r, s, a.ybf16 != 0);
+        store_y(y, (int64_t)m * a.ldy + r0 + r, s, a.ybf16 != 0);
     }
 }
 
@@ -258,6 +259,7 @@ GemvPlan plan_gemv(int mt, int64_t N, int64_t K, int grid) {
     p.mt = mt;
     GemvArgs &a = p.args;
     a.N = N;
+    a.ldy = N;
     a.K = K;
     a.P = (int)(K / 64);
     a.C = (a.P + kChunkPairs - 1) / kChunkPairs;
@@ -326,6 +328,7 @@ struct Limits {
 
 struct Args {
     int64_t N, K;
+    int64_t ldy;  // row stride of y
     int P, c, T, R, S, rowbytes, H, mrows, ybf16;
     uint32_t stage_bytes, off_x, off_bars, off_part;
 };
@@ -653,7 +656,7 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
         if (rr >= stage_rows(i)) continue;
         float sum = 0.f;
         for (int h = 0; h < a.H; ++h) sum += part[((size_t)lr * a.H + h) * MT + m];
-        store_y(y, (int64_t)m * a.N + stage_row0(i) + rr, sum, a.ybf16 != 0);
+        store_y(y, (int64_t)m * a.ldy + stage_row0(i) + rr, sum, a.ybf16 != 0);
     }
 }
 
@@ -670,6 +673,7 @@ Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
     Plan p{};
     Args &a = p.a;
     a.N = N;
+    a.ldy = N;
     a.K = K;
     a.P = (int)(K / 64);
     p.ok = (K % 1024 == 0);
@@ -707,71 +711,98 @@ Plan make_plan(int mt, int64_t N, int64_t K, int grid) {
     return p;
 }
 
+// One launch over n weight rows (all M = MT rows of x); y has row stride ldy.
 template <int MT>
-cudaError_t launch(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
-                   int sms, cudaStream_t s, unsigned int *err, bool *done) {
-    *done = false;
-    const int grid = (int)(N < sms ? N : sms);
-    Plan p = make_plan(MT, N, K, grid);
-    if (!p.ok) return cudaSuccess;
+cudaError_t launch(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t n, int64_t ldy,
+                   int64_t K, int sms, cudaStream_t s, unsigned int *err) {
+    const int grid = (int)(n < sms ? n : sms);
+    Plan p = make_plan(MT, n, K, grid);
+    if (!p.ok) return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_dp4a_kernel<MT>), (int)p.smem);
     if (e != cudaSuccess) return e;
     p.a.ybf16 = ybf16 ? 1 : 0;
-    for (int64_t m0 = 0; m0 < M; m0 += MT) {
-        p.a.mrows = (int)(M - m0 < MT ? M - m0 : MT);
-        e = launch_pdl(gemv_dp4a_kernel<MT>, dim3(grid), dim3(p.threads), p.smem, s, x + m0 * K, wq,
-                       y_offset(y, m0 * N, ybf16), p.a, err);
-        if (e != cudaSuccess) return e;
-    }
-    *done = true;
-    return cudaSuccess;
+    p.a.mrows = MT;
+    p.a.ldy = ldy;
+    return launch_pdl(gemv_dp4a_kernel<MT>, dim3(grid), dim3(p.threads), p.smem, s, x, wq, y, p.a, err);
 }
+
+bool fits(int mt, int64_t n, int64_t K, int sms) { return make_plan(mt, n, K, (int)(n < sms ? n : sms)).ok; }
 
 }  // namespace dp
 
 }  // namespace
 
+// The largest share of N (N halved until it fits) whose plan fits shared
+// memory: the per-row partial sums a CTA keeps grow with the rows it owns, so
+// a very tall matrix runs as several launches.  0 when none fits.
+template <class Fits>
+int64_t rows_per_launch(int64_t N, Fits fits) {
+    for (int64_t n = N;; n = (n + 1) / 2) {
+        if (fits(n)) return n;
+        if (n == 1) return 0;
+    }
+}
+
+// M <= 2 with K up to this runs on the CUDA cores (x of one row is held in
+// shared memory); larger K goes to the tensor-core decode, which streams x.
+constexpr int64_t kDecodeMaxK = 65536;
+
+bool decode_on_tensor_cores(int64_t M, int64_t K) { return M >= 3 || K > kDecodeMaxK; }
+
 size_t gemv_workspace_bytes(int64_t M, int64_t K) {
-    return M >= 3 && M <= 32 ? gemv_tc_workspace_bytes(M, K) : 0;
+    return M >= 1 && M <= 32 && decode_on_tensor_cores(M, K) ? gemv_tc_workspace_bytes(M, K) : 0;
+}
+
+// The tensor-core decode puts the 128-row weight tiles in gridDim.y; the
+// CUDA-core kernels cover any N (several launches when needed).
+bool gemv_shape_supported(int64_t M, int64_t N, int64_t K) {
+    return !decode_on_tensor_cores(M, K) || (N + 127) / 128 <= 65535;
 }
 
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
+    // three or more rows of x (or a K too long to hold in shared memory): the
+    // dot product moves to the tensor cores
+    if (decode_on_tensor_cores(M, K)) return launch_gemv_tc(x, wq, y, ybf16, M, N, K, workspace, s, err);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count(dev);
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const int64_t grid64 = (N + 1) / 2 < sms ? (N + 1) / 2 : sms;
-    const int grid = (int)grid64;
-    if (M <= 2) {
-        bool done = false;
-        e = M == 1 ? dp::launch<1>(x, wq, y, ybf16, M, N, K, sms, s, err, &done)
-                   : dp::launch<2>(x, wq, y, ybf16, M, N, K, sms, s, err, &done);
-        if (e != cudaSuccess || done) return e;
-    } else {
-        // three or more rows of x: the dot product moves to the tensor cores
-        return launch_gemv_tc(x, wq, y, ybf16, M, N, K, workspace, s, err);
-    }
-    // rows of x per launch: the largest power of two <= 8 that covers M (or
-    // fits shared memory); each launch streams the weights once
-    int mt = 1;
-    while (mt < 8 && mt < M) mt *= 2;
-    while (mt > 1 && plan_gemv(mt, N, K, grid).smem > kSmemLimit) mt /= 2;
-    if (plan_gemv(mt, N, K, grid).smem > kSmemLimit) return cudaErrorInvalidValue;
-    for (int64_t m0 = 0; m0 < M; m0 += mt) {
-        GemvPlan p = plan_gemv(mt, N, K, grid);
-        p.args.mrows = (int)((M - m0) < mt ? (M - m0) : mt);
-        p.args.ybf16 = ybf16 ? 1 : 0;
-        const uint16_t *xm = x + m0 * K;
-        float *ym = y_offset(y, m0 * N, ybf16);
-        switch (mt) {
-            case 1: e = launch_mt<1>(xm, wq, ym, p, grid, s, err); break;
-            case 2: e = launch_mt<2>(xm, wq, ym, p, grid, s, err); break;
-            case 4: e = launch_mt<4>(xm, wq, ym, p, grid, s, err); break;
-            default: e = launch_mt<8>(xm, wq, ym, p, grid, s, err); break;
+    const int64_t rowbytes = K / 32 * 18;
+    auto grid_for = [&](int64_t n) { return (int)(n < sms ? n : sms); };
+    // the integer-dot kernel (both rows of x in one pass over the weights)
+    const int mt_dp = (int)M;
+    const int64_t ndp = rows_per_launch(N, [&](int64_t n) { return dp::fits(mt_dp, n, K, sms); });
+    if (ndp > 0) {
+        for (int64_t n0 = 0; n0 < N; n0 += ndp) {
+            const int64_t n = N - n0 < ndp ? N - n0 : ndp;
+            e = M == 1 ? dp::launch<1>(x, wq + n0 * rowbytes, y_offset(y, n0, ybf16), ybf16, n, N, K, sms, s, err)
+                       : dp::launch<2>(x, wq + n0 * rowbytes, y_offset(y, n0, ybf16), ybf16, n, N, K, sms, s, err);
+            if (e != cudaSuccess) return e;
         }
-        if (e != cudaSuccess) return e;
+        return cudaSuccess;
+    }
+    // the binary16 kernel (K % 1024 != 0, or a K the integer kernel's
+    // threads cannot cover): both rows of x per pass where they fit
+    const int64_t ng =
+        rows_per_launch(N, [&](int64_t n) { return plan_gemv(1, n, K, grid_for(n)).smem <= kSmemLimit; });
+    if (ng == 0) return cudaErrorInvalidValue;
+    for (int64_t n0 = 0; n0 < N; n0 += ng) {
+        const int64_t n = N - n0 < ng ? N - n0 : ng;
+        const int grid = grid_for(n);
+        const int mt = M == 2 && plan_gemv(2, n, K, grid).smem <= kSmemLimit ? 2 : 1;
+        for (int64_t m0 = 0; m0 < M; m0 += mt) {
+            GemvPlan p = plan_gemv(mt, n, K, grid);
+            p.args.mrows = (int)((M - m0) < mt ? (M - m0) : mt);
+            p.args.ybf16 = ybf16 ? 1 : 0;
+            p.args.ldy = N;
+            const uint16_t *xm = x + m0 * K;
+            float *ym = y_offset(y, m0 * N + n0, ybf16);
+            e = mt == 1 ? launch_mt<1>(xm, wq + n0 * rowbytes, ym, p, grid, s, err)
+                        : launch_mt<2>(xm, wq + n0 * rowbytes, ym, p, grid, s, err);
+            if (e != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }

@@ -45,15 +45,18 @@ inline float *y_offset(float *y, int64_t elems, bool ybf16) {
 }
 
 // Decode GEMV for M <= 32 (x, y point at row 0; row strides K and N).
-// `workspace` (256-byte aligned, gemv_workspace_bytes(M, K) bytes) is used for
-// 3 <= M <= 32 only.
+// `workspace` (256-byte aligned, gemv_workspace_bytes(M, K) bytes) is used
+// by the tensor-core decode only: 3 <= M <= 32, or M <= 2 with K > 65536.
+// gemv_shape_supported: the launch grids of the path the shape takes stay
+// within the device limits.
 size_t gemv_workspace_bytes(int64_t M, int64_t K);
+bool gemv_shape_supported(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, cudaStream_t s, unsigned int *err);
 
-// Tensor-core decode for 3 <= M <= 32: x rounded once into binary16 MMA
-// tiles in `xtiles` (gemv_tc_workspace_bytes(M, K) bytes), then split-K over
-// a thread-block cluster.
+// Tensor-core decode for M <= 32: x rounded once into binary16 MMA tiles in
+// the workspace (gemv_tc_workspace_bytes(M, K) bytes, which also holds the
+// split-K partial tiles and counters).  N <= 65535 * 128.
 size_t gemv_tc_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                            int64_t K, void *xtiles, cudaStream_t s, unsigned int *err);
@@ -71,6 +74,7 @@ cudaError_t launch_pad(const uint16_t *x, const uint8_t *wq, int64_t M, int64_t 
 // split (splits > 1), the fp32 partial tiles: gemm_workspace_bytes(M, N, K,
 // splits) bytes.  gemm_splits picks the split for a device with `sms` SMs.
 int gemm_splits(int64_t M, int64_t N, int64_t K, int sms);
+bool gemm_shape_supported(int64_t M, int64_t N, int64_t K);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
 cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, int splits, cudaStream_t s, unsigned int *err);

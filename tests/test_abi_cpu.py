@@ -72,6 +72,12 @@ def test_workspace_sizes(lib):
     assert lib.q4_0_matmul_workspace_bytes(64, 300, 288) >= a256(300 * 16 * 18) + a256(64 * 512 * 2) + 64 * 512 * 2
     assert lib.q4_0_matmul_workspace_bytes(33, 5120, 5120) == 33 * 5120 * 2
     assert lib.q4_0_gemm_workspace_bytes(3, 128, 256) % 256 == 0
+    # one or two rows with K past 65536 (x no longer fits shared memory) take
+    # the tensor-core decode and its x tiles
+    for M in (1, 2):
+        assert lib.q4_0_matmul_workspace_bytes(M, 300, 65536) == 0
+        assert lib.q4_0_matmul_workspace_bytes(M, 300, 65792) == 16 * 65792 * 2
+        assert lib.q4_0_gemv_workspace_bytes(M, 131072) == 16 * 131072 * 2
 
 
 def test_invalid_arguments_rejected_before_cuda(lib):
@@ -95,6 +101,19 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.q4_0_quantize(None, good, 1, 32, None) == -1
     assert lib.q4_0_quantize(good, good, 1, 31, None) == -1
     assert lib.q4_0_device_error(None) == -1
+
+
+def test_shapes_past_the_grid_limits_are_unsupported(lib):
+    """Shapes the launch grids cannot hold are refused before any CUDA call:
+    the tensor-core decode's weight tiles (N <= 65535 * 128) and the GEMM's
+    x tiles (at most 65535)."""
+    good = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 21)
+    assert lib.q4_0_matmul_ws(good, good, good, 16, 65535 * 128 + 1, 256, ws, 1 << 40, None) == -2
+    assert lib.q4_0_matmul_ws(good, good, good, 1, 65535 * 128 + 1, 65792, ws, 1 << 40, None) == -2
+    assert lib.q4_0_matmul_ws(good, good, good, 1 << 25, 128, 256, ws, 1 << 40, None) == -2
+    assert lib.q4_0_gemv_ws(good, good, good, 16, 65535 * 128 + 1, 256, ws, 1 << 40, None) == -2
+    assert lib.q4_0_gemm(good, good, good, 1 << 25, 128, 256, ws, 1 << 40, None) == -2
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
