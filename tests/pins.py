@@ -141,11 +141,14 @@ def pin_f16_encode_sampled(o, n=1 << 22, seed=7):
     assert np.array_equal(got[~np.isnan(sub)], ref[~np.isnan(sub)])
 
 
-def pin_f16_encode_exhaustive(o, chunk_log2=26):
-    """All 2^31 non-negative binary32 patterns (the sign is a separate bit)."""
+def pin_f16_encode_exhaustive(o, chunk_log2=24):
+    """All 2^31 non-negative binary32 patterns (the sign is a separate bit),
+    in chunks written into one reused buffer."""
     step = 1 << chunk_log2
+    ramp = np.arange(step, dtype=np.uint32)
+    u = np.empty(step, dtype=np.uint32)
     for start in range(0, 1 << 31, step):
-        u = np.arange(start, start + step, dtype=np.uint64).astype(np.uint32)
+        np.add(ramp, np.uint32(start), out=u)
         _check_f16_encode(o, u.view(np.float32))
 
 
