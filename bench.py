@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--layers", type=int, default=8, help="resident layer copies (decode/batched)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--grouped", action="store_true",
+                   help="decode (M = 1): each layer's matrices as one q4_0_matmul_grouped call")
     p.add_argument("--y-dtype", choices=["f32", "bf16"], default="f32",
                    help="element type of y (bf16: the rounded-once output of q4_0_matmul_ex)")
     return p.parse_args()
@@ -223,9 +225,18 @@ def run_ours(args, rank, world, local):
     step_flops = per_step_layers * sum(2.0 * M * N * K for _, (N, K) in shapes)
     step_weights = per_step_layers * sum(N * K for _, (N, K) in shapes)
 
+    Ns = [N for _, (N, K) in shapes]
+    Ks = [K for _, (N, K) in shapes]
+    grouped = args.grouped and q4.grouped_launches(M, Ns, Ks) > 0
+    if args.grouped and not grouped:
+        raise SystemExit("--grouped: the grouped decode does not take these shapes at this M")
+
     def enqueue_step(i):
         ls = range(layers) if sweep else (i % layers,)
         for l in ls:
+            if grouped:
+                q4.matmul_grouped(xs, wq[l], Ns, Ks, outs=ys, stream=stream, out_dtype=ydt)
+                continue
             for j, (_, (N, K)) in enumerate(shapes):
                 q4.matmul(xs[j], wq[l][j], N, K, out=ys[j], workspace=wss[j], stream=stream, out_dtype=ydt)
 
@@ -248,7 +259,10 @@ def run_ours(args, rank, world, local):
             for v in range(cycle):
                 enqueue_step(v)
     calls_per_step = len(shapes) * (layers if sweep else 1)
-    launches_per_step = sum(kernels_per_call(q4, M, N, K) for _, (N, K) in shapes) * (layers if sweep else 1)
+    if grouped:
+        launches_per_step = q4.grouped_launches(M, Ns, Ks) * (layers if sweep else 1)
+    else:
+        launches_per_step = sum(kernels_per_call(q4, M, N, K) for _, (N, K) in shapes) * (layers if sweep else 1)
 
     def run_steps(n):
         for _ in range(n // cycle):
@@ -307,6 +321,15 @@ def run_ours(args, rank, world, local):
         for i in range(e2e_steps):
             ls = range(layers) if sweep else (i % layers,)
             for l in ls:
+                if grouped:
+                    # the grouped call takes device buffers: x copied in and
+                    # y copied out around it, on the same stream
+                    for j in range(len(shapes)):
+                        xs[j].copy_(x_host[j], non_blocking=True)
+                    q4.matmul_grouped(xs, wq[l], Ns, Ks, outs=ys, stream=stream, out_dtype=ydt)
+                    for j in range(len(shapes)):
+                        y_host[j].copy_(ys[j], non_blocking=True)
+                    continue
                 for j, (_, (N, K)) in enumerate(shapes):
                     q4.matmul_host(x_host[j], wq[l][j], N, K, out=y_host[j], workspace=whs[j], stream=stream,
                                    out_dtype=ydt)
@@ -319,11 +342,13 @@ def run_ours(args, rank, world, local):
     value = gbs if M < 256 else tflops
     # roofline of the dominant kernel (the only kernel in the timed region)
     launches = args.steps * launches_per_step
+    if grouped:
+        calls_per_step = launches_per_step  # one grouped launch covers several matmuls
     calls = args.steps * calls_per_step  # launches of the dominant kernel (one per matmul)
     if M < 256:
         roof = {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(gbs / world / hbm, 4), "traffic": None,
-                "kernel": dominant_kernel(M), "peak_source": peak_kind,
+                "kernel": dominant_kernel(M, grouped), "peak_source": peak_kind,
                 "bytes_per_launch": round(step_bytes / calls_per_step),
                 "avg_launch_us": round(ms_local * 1e3 / calls, 3)}
     else:
@@ -331,7 +356,7 @@ def run_ours(args, rank, world, local):
                 "unit": "TFLOP/s", "frac": round(tflops / world / tf_sust, 4), "traffic": None,
                 "kernel": dominant_kernel(M), "peak_source": peak_kind + " sustained",
                 "avg_launch_us": round(ms_local * 1e3 / calls, 3)}
-    traffic = load_traffic(args.workload, M)
+    traffic = None if grouped else load_traffic(args.workload, M)
     if traffic is not None:
         roof["traffic"] = traffic
 
@@ -342,7 +367,7 @@ def run_ours(args, rank, world, local):
         "dtype": ("q4_0 codes x 15-bit fixed-point x: int dp4a in-block, f32 across blocks" if M <= 2 else
                   "q4_0 weights -> f16 tiles; f16 MMA, f32 accumulate"),
         "data": "synthetic: W ~ N(0, 0.02) quantized on device, x ~ N(0, 1) bf16",
-        "config": {"workload": workload_name(args.workload, M, layers), "M": M,
+        "config": {"workload": workload_name(args.workload, M, layers, grouped), "M": M,
                    "shapes": {s: list(nk) for s, nk in shapes}, "layer_copies": layers,
                    "l2": "inputs larger than L2: %d resident layer copies, %.2f GB cycled"
                          % (layers, layers * sum(0.5625 * N * K for _, (N, K) in shapes) / 1e9),
@@ -361,7 +386,11 @@ def run_ours(args, rank, world, local):
     return line if rank == 0 else None
 
 
-def workload_name(w, M, layers):
+def workload_name(w, M, layers, grouped=False):
+    if grouped:
+        return (f"decode M={M}, four 27B-class layer matrices per step as one grouped call, "
+                f"{layers} layer copies" if w != "sweep" else
+                f"64-layer decode sweep at M={M}, each layer's four matrices as one grouped call")
     return {"decode": f"decode M={M}, four 27B-class layer matrices per step, {layers} layer copies",
             "batched": f"batched decode M={M}, four 27B-class layer matrices per step, {layers} layer copies",
             "prefill": f"prefill M={M}, four 27B-class layer matrices per step",
@@ -382,7 +411,9 @@ def kernels_per_call(q4, M, N, K):
     return 3 if q4.lib().q4_0_gemm_workspace_bytes(M, N, K) > x16 else 2
 
 
-def dominant_kernel(M):
+def dominant_kernel(M, grouped=False):
+    if grouped:
+        return f"gemv_dp4a_grouped_kernel<{M}>"
     if M <= 2:
         return f"gemv_dp4a_kernel<{M}>"
     if M <= 32:

@@ -188,6 +188,34 @@ int q4_0_matmul_host(const uint16_t *x_host, const uint8_t *wq, void *y_host, in
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * q4_0_matmul_grouped -- G independent problems y_g = x_g * W_g^T that share
+ * M, issued together on `stream`:
+ *   G        : 0 .. 4096 problems (0 does nothing).
+ *   x, wq, y : host arrays of G device pointers; x_g bf16 [M][K_g], wq_g
+ *              Q4_0 [N_g][K_g], y_g [M][N_g] of `y_type` (Q4_0_Y_F32 or
+ *              Q4_0_Y_BF16), each as in q4_0_matmul_ex.  The arrays are
+ *              read during the call only.
+ *   N, K     : host arrays of the G sizes.
+ * With M == 1 and K_g % 1024 == 0 (K_g <= 65536), consecutive problems run
+ * as one persistent decode launch per group of up to eight (as many as one
+ * SM's shared memory holds): every CTA streams its share of each problem's
+ * weights back to back, so the launch front and tail are paid once per group
+ * rather than once per matrix.  Any other problem runs as q4_0_matmul_ex
+ * with library-allocated scratch (cudaMallocAsync on `stream`), in order.
+ * Each y_g equals the q4_0_matmul_ex result of its problem bit for bit.
+ * Every problem is checked before anything is launched.  The problems must
+ * not overlap in y with each other or with any x or W.
+ * Returns Q4_0_OK, Q4_0_ERR_INVALID_ARG, Q4_0_ERR_UNSUPPORTED or Q4_0_ERR_CUDA.
+ */
+int q4_0_matmul_grouped(int G, const uint16_t *const *x, const uint8_t *const *wq, void *const *y, int y_type,
+                        int64_t M, const int64_t *N, const int64_t *K, void *stream);
+
+/* Kernel launches a q4_0_matmul_grouped call with these sizes makes on the
+ * current device when the grouped decode takes every problem; -1 when it
+ * does not take them all (or there is no device). */
+int q4_0_matmul_grouped_launches(int G, int64_t M, const int64_t *N, const int64_t *K);
+
+/*
  * q4_0_gemv -- the decode kernels alone (what q4_0_matmul runs for
  * M <= 32).  Same arguments, layout and result contract as q4_0_matmul;
  * M <= 32 (larger M is UNSUPPORTED).  M <= 2 with K <= 65536 needs no

@@ -39,6 +39,8 @@ SIGNATURES = {
     "q4_0_matmul_ex": ([_P, _P, _P, _INT, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_matmul_host_workspace_bytes": ([_I64, _I64, _I64, _INT], _SZ),
     "q4_0_matmul_host": ([_P, _P, _P, _INT, _I64, _I64, _I64, _P, _SZ, _P], _INT),
+    "q4_0_matmul_grouped": ([_INT, _P, _P, _P, _INT, _I64, _P, _P, _P], _INT),
+    "q4_0_matmul_grouped_launches": ([_INT, _I64, _P, _P], _INT),
     "q4_0_gemv": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "q4_0_gemv_workspace_bytes": ([_I64, _I64], _SZ),
     "q4_0_gemv_ws": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
@@ -222,6 +224,47 @@ def matmul_host(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Te
                                   ws.data_ptr() if ws is not None else None, wsb, _stream(stream)),
            "q4_0_matmul_host")
     return out
+
+
+def matmul_grouped(xs, wqs, Ns, Ks, outs=None, stream=None, out_dtype=torch.float32):
+    """y_g = x_g W_g^T for independent problems sharing M, through
+    q4_0_matmul_grouped (one persistent decode launch per group where the
+    problems allow it).  Returns the list of outputs."""
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+    G = len(xs)
+    if not (len(wqs) == len(Ns) == len(Ks) == G):
+        raise ValueError("xs, wqs, Ns and Ks must have the same length")
+    outs = list(outs) if outs is not None else [None] * G
+    if len(outs) != G:
+        raise ValueError("outs must have one tensor per problem")
+    M, ys = None, []
+    for x, wq, N, K, out in zip(xs, wqs, Ns, Ks, outs):
+        m, out = _mm_args(x, wq, N, K, out, out_dtype)
+        if M is None:
+            M = m
+        elif m != M:
+            raise ValueError("every x must have the same number of rows")
+        ys.append(out)
+    if G == 0:
+        return ys
+    ptrs = lambda ts: ctypes.cast((ctypes.c_void_p * G)(*[t.data_ptr() for t in ts]), ctypes.c_void_p)
+    sizes = lambda vs: ctypes.cast((ctypes.c_int64 * G)(*[int(v) for v in vs]), ctypes.c_void_p)
+    xa, wa, ya, na, ka = ptrs(xs), ptrs(wqs), ptrs(ys), sizes(Ns), sizes(Ks)
+    yt = Y_BF16 if out_dtype == torch.bfloat16 else Y_F32
+    _check(lib().q4_0_matmul_grouped(G, xa, wa, ya, yt, M, na, ka, _stream(stream)), "q4_0_matmul_grouped")
+    return ys
+
+
+def grouped_launches(M: int, Ns, Ks) -> int:
+    """Kernel launches of a matmul_grouped call with these sizes when the
+    grouped decode takes every problem, else -1 (q4_0_matmul_grouped_launches)."""
+    G = len(Ns)
+    if G == 0 or len(Ks) != G:
+        return -1
+    na = ctypes.cast((ctypes.c_int64 * G)(*[int(v) for v in Ns]), ctypes.c_void_p)
+    ka = ctypes.cast((ctypes.c_int64 * G)(*[int(v) for v in Ks]), ctypes.c_void_p)
+    return int(lib().q4_0_matmul_grouped_launches(G, M, na, ka))
 
 
 def host_workspace_bytes(M: int, N: int, K: int, out_dtype=torch.float32) -> int:

@@ -299,6 +299,50 @@ int q4_0_matmul_ex(const uint16_t *x, const uint8_t *wq, void *y, int y_type, in
     return matmul_ws_impl(x, wq, yf, bf16, M, N, K, workspace, workspace_bytes, stream);
 }
 
+int q4_0_matmul_grouped(int G, const uint16_t *const *x, const uint8_t *const *wq, void *const *y, int y_type,
+                        int64_t M, const int64_t *N, const int64_t *K, void *stream) {
+    if (G < 0 || G > 4096) return Q4_0_ERR_INVALID_ARG;
+    if (G == 0) return Q4_0_OK;
+    if (!x || !wq || !y || !N || !K) return Q4_0_ERR_INVALID_ARG;
+    if (y_type != Q4_0_Y_F32 && y_type != Q4_0_Y_BF16) return Q4_0_ERR_INVALID_ARG;
+    // every problem is checked before anything is launched
+    for (int g = 0; g < G; ++g) {
+        const int st = check_matmul_args(x[g], wq[g], y[g], M, N[g], K[g], true);
+        if (st != Q4_0_OK) return st;
+        const int64_t kk = K[g] % 256 != 0 ? padded_k(K[g]) : K[g];
+        if (M <= 32 ? !gemv_shape_supported(M, N[g], kk) : !gemm_shape_supported(M, N[g], kk))
+            return Q4_0_ERR_UNSUPPORTED;
+    }
+    unsigned int *err = device_error_word();
+    if (!err) return Q4_0_ERR_CUDA;
+    const bool bf16 = y_type == Q4_0_Y_BF16;
+    float *const *yf = reinterpret_cast<float *const *>(y);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // runs of problems the grouped decode takes go out together; any other
+    // problem is one q4_0_matmul_ex call, in order
+    for (int g = 0; g < G;) {
+        int e = g;
+        while (e < G && grouped_decode_eligible(M, N[e], K[e])) ++e;
+        if (e > g) {
+            const int st = from_cuda(launch_gemv_grouped(e - g, x + g, wq + g, yf + g, bf16, M, N + g, K + g, s, err));
+            if (st != Q4_0_OK) return st;
+            g = e;
+            continue;
+        }
+        const int st = q4_0_matmul_ex(x[g], wq[g], y[g], y_type, M, N[g], K[g], nullptr, 0, stream);
+        if (st != Q4_0_OK) return st;
+        ++g;
+    }
+    return Q4_0_OK;
+}
+
+int q4_0_matmul_grouped_launches(int G, int64_t M, const int64_t *N, const int64_t *K) {
+    if (G < 1 || G > 4096 || !N || !K) return -1;
+    for (int g = 0; g < G; ++g)
+        if (N[g] < 1 || K[g] < 32 || K[g] % 32 != 0 || !grouped_decode_eligible(M, N[g], K[g])) return -1;
+    return grouped_decode_launches(G, M, N, K);
+}
+
 size_t q4_0_matmul_host_workspace_bytes(int64_t M, int64_t N, int64_t K, int y_type) {
     if (y_type != Q4_0_Y_F32 && y_type != Q4_0_Y_BF16) return 0;
     if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return 0;

@@ -728,6 +728,353 @@ cudaError_t launch(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, i
 
 bool fits(int mt, int64_t n, int64_t K, int sms) { return make_plan(mt, n, K, (int)(n < sms ? n : sms)).ok; }
 
+// ---------------------------------------------------------------------------
+// Grouped decode: up to kMaxGroup independent problems y_g = x_g W_g^T (one
+// row of x each, each K_g % 1024 == 0) in one launch.  Every CTA owns the same share
+// of rows of each problem; one producer ring streams the problems' stages
+// back to back, so a step of several matrices pays the per-launch front
+// (dependency release, x conversion) and tail (row sums) once instead of
+// once per matrix.  x of every problem is converted at the start; each
+// thread reloads its x registers when the stream moves on to the next
+// problem.  Per row the arithmetic and the summation order are those of
+// gemv_dp4a_kernel, so results equal the one-problem calls bit for bit.
+// ---------------------------------------------------------------------------
+constexpr int kMaxGroup = 8;
+
+struct GroupItem {
+    const uint16_t *x;
+    const uint8_t *wq;
+    float *y;   // element type per GroupArgs::ybf16
+    int64_t N;
+    int P, c, R, H, rowbytes;
+    uint32_t off_x, off_part;  // this problem's x records and row partials in shared memory
+};
+
+struct GroupArgs {
+    int G, S, T, mrows, ybf16;
+    uint32_t slot_bytes, off_bars;
+    GroupItem it[kMaxGroup];
+};
+
+template <int MT>
+__global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
+    gemv_dp4a_grouped_kernel(const __grid_constant__ GroupArgs a, unsigned int *err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bars);
+    uint64_t *empty = full + a.S;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + a.S);
+    uint64_t *xready = empty + a.S + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nwc = a.T >> 5;
+    // this CTA's rows [r0, r1) of problem g and their stage count
+    auto rows_of = [&](int g, int64_t &r0, int64_t &r1) {
+        r0 = (int64_t)blockIdx.x * a.it[g].N / gridDim.x;
+        r1 = (int64_t)(blockIdx.x + 1) * a.it[g].N / gridDim.x;
+    };
+    auto stages_of = [&](int g) -> int {
+        int64_t r0, r1;
+        rows_of(g, r0, r1);
+        return (int)((r1 - r0 + a.it[g].R - 1) / a.it[g].R);
+    };
+
+    if (warp == nwc && lane == 0) {
+        for (int i = 0; i < a.S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], nwc);
+        }
+        mbar_init(xready, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == nwc) {
+        // the stages of all problems in order, as the compute threads take them
+        if (lane == 0) {
+            const uint64_t policy = l2_evict_first_policy();
+            struct Cursor {
+                int g, i, nst;
+                int64_t r0, r1;
+            };
+            auto seek = [&](Cursor &c) {  // first stage at or after (g, i)
+                while (c.g < a.G) {
+                    if (c.i == 0) {
+                        rows_of(c.g, c.r0, c.r1);
+                        c.nst = stages_of(c.g);
+                    }
+                    if (c.i < c.nst) return;
+                    ++c.g;
+                    c.i = 0;
+                }
+            };
+            auto next = [&](Cursor &c) {
+                ++c.i;
+                seek(c);
+            };
+            auto stage = [&](const Cursor &c, int64_t &row, uint32_t &bytes) {
+                const GroupItem &p = a.it[c.g];
+                row = c.r0 + (int64_t)c.i * p.R;
+                bytes = (uint32_t)(c.r1 - row < p.R ? c.r1 - row : p.R) * (uint32_t)p.rowbytes;
+            };
+            int total = 0;
+            for (int g = 0; g < a.G; ++g) total += stages_of(g);
+            Cursor cur{0, 0, 0, 0, 0};
+            seek(cur);
+            int j = 0;  // stages issued
+            auto issue = [&]() {
+                int64_t row;
+                uint32_t bytes;
+                stage(cur, row, bytes);
+                const int s = j % a.S;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                bulk_g2s_hint(smem + (size_t)s * a.slot_bytes, a.it[cur.g].wq + row * a.it[cur.g].rowbytes, bytes,
+                              &full[s], policy);
+                ++j;
+                next(cur);
+            };
+            // as in the one-problem kernel: the first stages before the
+            // dependency wait, the rest of the first ring fill into L2
+            constexpr int kPreWait = 3;
+            const int pre = min(kPreWait, min(a.S, total));
+            while (j < pre) issue();
+            if (MT == 1) {
+                Cursor c = cur;
+                for (int k = j; k < a.S && k < total; ++k) {
+                    int64_t row;
+                    uint32_t bytes;
+                    stage(c, row, bytes);
+                    bulk_prefetch_l2(a.it[c.g].wq + row * a.it[c.g].rowbytes, bytes, policy);
+                    next(c);
+                }
+            }
+            pdl_wait();
+            mbar_wait(xready, 0, abort_flag, err);
+            while (j < a.S && j < total) issue();
+            while (j < total) {
+                if (!mbar_wait(&empty[j % a.S], ((j / a.S) & 1) ^ 1, abort_flag, err)) break;
+                issue();
+            }
+            for (int i = max(0, j - a.S); i < j; ++i) mbar_drain(&full[i % a.S], (i / a.S) & 1);
+        }
+        return;
+    }
+
+    // x of every problem -> fixed point in its records
+    pdl_wait();
+    constexpr int kParts = 4;
+    static_assert(MT <= 2, "the row of a block is blk_id >= nb");
+    for (int g = 0; g < a.G; ++g) {
+        const GroupItem &p = a.it[g];
+        uint32_t *xsm = reinterpret_cast<uint32_t *>(smem + p.off_x);
+        const int nb = 2 * p.P, nparts = 2 * MT * nb;
+        const int64_t K = (int64_t)p.P * 64;
+        for (int t0 = tid - lane; t0 < nparts; t0 += kParts * a.T) {
+            uint4 u[kParts][2];
+#pragma unroll
+            for (int k = 0; k < kParts; ++k) {
+                if (t0 + k * a.T < nparts) {
+                    const int t = t0 + k * a.T + lane;
+                    const int q = t < nparts ? t : nparts - 1;
+                    const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0;
+                    load_part(m < a.mrows ? p.x + (int64_t)m * K : nullptr, blk_id - m * nb, q & 1, t < nparts,
+                              u[k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kParts; ++k) {
+                if (t0 + k * a.T < nparts) {
+                    const int t = t0 + k * a.T + lane;
+                    const int q = t < nparts ? t : nparts - 1;
+                    const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0, b = blk_id - m * nb;
+                    convert_part(u[k], b, q & 1, t < nparts, xsm + ((size_t)m * p.P + (b >> 1)) * kPairWords);
+                }
+            }
+        }
+    }
+    named_bar_sync(1, a.T);
+    if (tid == 0) mbar_arrive(xready);
+
+    constexpr int G = Limits<MT>::kG, kRed = Limits<MT>::kRed;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int g = 0; g < a.G && ok; ++g) {
+        const GroupItem &p = a.it[g];
+        int64_t r0, r1;
+        rows_of(g, r0, r1);
+        const int nst = (int)((r1 - r0 + p.R - 1) / p.R);
+        if (nst == 0) continue;
+        // thread (rs, tc) owns block pairs tc + gg TPR of row slot rs of this problem
+        const int tpr = p.P / G;
+        const int tc = tid % tpr, rs = tid / tpr;
+        const bool active = rs < p.c;
+        const uint32_t *xsm = reinterpret_cast<const uint32_t *>(smem + p.off_x);
+        XReg<MT> xr[G];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const uint4 *rec =
+                    reinterpret_cast<const uint4 *>(xsm + ((size_t)m * p.P + tc + gg * tpr) * kPairWords);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 u = rec[i], w = rec[4 + i];
+                    xr[gg].h[m][4 * i] = u.x; xr[gg].h[m][4 * i + 1] = u.y;
+                    xr[gg].h[m][4 * i + 2] = u.z; xr[gg].h[m][4 * i + 3] = u.w;
+                    xr[gg].l[m][4 * i] = w.x; xr[gg].l[m][4 * i + 1] = w.y;
+                    xr[gg].l[m][4 * i + 2] = w.z; xr[gg].l[m][4 * i + 3] = w.w;
+                }
+                const uint4 t = rec[8];
+                xr[gg].ncorr[m][0] = (int)t.x;
+                xr[gg].ncorr[m][1] = (int)t.y;
+                xr[gg].xs[m][0] = __uint_as_float(t.z);
+                xr[gg].xs[m][1] = __uint_as_float(t.w);
+            }
+        }
+        const int last_rows = (int)(r1 - r0 - (int64_t)(nst - 1) * p.R);
+        const uint8_t *my_row = smem + (size_t)rs * p.rowbytes + tc * 36;
+        float *my_part = reinterpret_cast<float *>(smem + p.off_part) + ((size_t)rs * p.H + tc / kRed) * MT;
+        const int part_step = p.R * p.H * MT;
+        for (int i = 0; i < nst; ++i) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag, err))) {
+                ok = false;
+                break;
+            }
+            const int rows = i == nst - 1 ? last_rows : p.R;
+            const bool valid = active && rs < rows;
+            uint32_t wv[G][9];
+            if (valid) {
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) {
+                    const uint32_t *src =
+                        reinterpret_cast<const uint32_t *>(my_row + (uint32_t)s * a.slot_bytes + gg * tpr * 36);
+#pragma unroll
+                    for (int k = 0; k < 9; ++k) wv[gg][k] = src[k];
+                }
+            }
+            float v[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) v[m] = 0.f;
+            if (valid) {
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) {
+                    const uint32_t *w = wv[gg];
+                    const uint32_t Q0[4] = {__funnelshift_r(w[0], w[1], 16), __funnelshift_r(w[1], w[2], 16),
+                                            __funnelshift_r(w[2], w[3], 16), __funnelshift_r(w[3], w[4], 16)};
+                    const uint32_t Q1[4] = {w[5], w[6], w[7], w[8]};
+                    block_dp<MT>(w[0] & 0xFFFFu, Q0, xr[gg], 0, v);
+                    block_dp<MT>(w[4] >> 16, Q1, xr[gg], 1, v);
+                }
+            }
+            // release the stage only once every lane has used its words
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float t = v[m];
+#pragma unroll
+                for (int o = kRed / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                v[m] = t;
+            }
+            if (valid && (lane & (kRed - 1)) == 0) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) my_part[m] = v[m];
+            }
+            my_part += part_step;
+            if (++s == a.S) {
+                s = 0;
+                ph ^= 1;
+            }
+        }
+    }
+    named_bar_sync(1, a.T);
+    // fixed-order sums over the P / 16 partials of every row of every problem
+    for (int g = 0; g < a.G; ++g) {
+        const GroupItem &p = a.it[g];
+        int64_t r0, r1;
+        rows_of(g, r0, r1);
+        const int nst = (int)((r1 - r0 + p.R - 1) / p.R);
+        const float *part = reinterpret_cast<const float *>(smem + p.off_part);
+        const int local_rows = nst * p.R;
+        for (int t = tid; t < local_rows * a.mrows; t += a.T) {
+            const int m = t / local_rows, lr = t - m * local_rows;
+            const int i = lr / p.R, rr = lr - i * p.R;
+            const int64_t row = r0 + (int64_t)i * p.R;
+            if (rr >= (int)(r1 - row < p.R ? r1 - row : p.R)) continue;
+            float sum = 0.f;
+            for (int h = 0; h < p.H; ++h) sum += part[((size_t)lr * p.H + h) * MT + m];
+            store_y(p.y, (int64_t)m * p.N + row + rr, sum, a.ybf16 != 0);
+        }
+    }
+}
+
+// Shared-memory plan of a group: the ring (S slots of the largest stage),
+// each problem's x records and row partials, the barriers.  false when the
+// problems do not fit with at least kMinGroupStages stages (a shallower ring
+// streams slower than splitting the group).
+bool plan_group(int mt, int grid, int G, const int64_t *N, const int64_t *K, GroupArgs &a, size_t &smem,
+                int &threads) {
+    const int max_threads = mt == 1 ? Limits<1>::kThreads : Limits<2>::kThreads;
+    const size_t smem_limit = mt == 1 ? Limits<1>::kSmem : Limits<2>::kSmem;
+    const int gsz = mt == 1 ? Limits<1>::kG : Limits<2>::kG;
+    const int budget = max_threads - 32;
+    a.G = G;
+    uint32_t slot = 0;
+    int T = 0;
+    size_t fixed = 0;
+    for (int g = 0; g < G; ++g) {
+        GroupItem &p = a.it[g];
+        if (K[g] % 1024 != 0 || N[g] < 1) return false;
+        p.N = N[g];
+        p.P = (int)(K[g] / 64);
+        const int tpr = p.P / gsz;
+        p.c = max(1, budget / tpr);
+        if (p.c * tpr > budget) return false;
+        T = max(T, ((p.c * tpr + 31) / 32) * 32);
+        p.R = p.c;
+        p.H = p.P / 16;
+        p.rowbytes = (int)(K[g] / 32 * 18);
+        slot = max(slot, (uint32_t)(p.R * p.rowbytes));
+        const int64_t rows_cap = ((N[g] + grid - 1) / grid + p.R) / p.R * p.R;
+        fixed += (size_t)mt * p.P * kPairWords * 4 + (size_t)rows_cap * p.H * mt * 4;
+    }
+    slot = (slot + 127) & ~127u;
+    constexpr int kMinGroupStages = 5;
+    int S = 8;
+    while (S > kMinGroupStages && (size_t)S * slot + fixed + 16 * 8 + 64 > smem_limit) --S;
+    size_t off = (size_t)S * slot;
+    for (int g = 0; g < G; ++g) {
+        GroupItem &p = a.it[g];
+        p.off_x = (uint32_t)off;
+        off += (size_t)mt * p.P * kPairWords * 4;
+    }
+    for (int g = 0; g < G; ++g) {
+        GroupItem &p = a.it[g];
+        p.off_part = (uint32_t)off;
+        const int64_t rows_cap = ((N[g] + grid - 1) / grid + p.R) / p.R * p.R;
+        off += (size_t)rows_cap * p.H * mt * 4;
+    }
+    off = (off + 15) & ~(size_t)15;
+    a.off_bars = (uint32_t)off;
+    off += (size_t)2 * S * 8 + 16;
+    a.S = S;
+    a.T = T;
+    a.slot_bytes = slot;
+    smem = off;
+    threads = T + 32;
+    return smem <= smem_limit && threads <= max_threads;
+}
+
+template <int MT>
+cudaError_t launch_group(const GroupArgs &a0, size_t smem, int threads, int grid, cudaStream_t s,
+                         unsigned int *err) {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_dp4a_grouped_kernel<MT>), (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(gemv_dp4a_grouped_kernel<MT>, dim3(grid), dim3(threads), smem, s, a0, err);
+}
+
 }  // namespace dp
 
 }  // namespace
@@ -757,6 +1104,95 @@ size_t gemv_workspace_bytes(int64_t M, int64_t K) {
 // CUDA-core kernels cover any N (several launches when needed).
 bool gemv_shape_supported(int64_t M, int64_t N, int64_t K) {
     return !decode_on_tensor_cores(M, K) || (N + 127) / 128 <= 65535;
+}
+
+namespace {
+int sm_count_or_zero() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return device_sm_count(dev);
+}
+}  // namespace
+
+// One row of x only: with two rows the grouped launches streamed slower than
+// one launch per matrix (2943-2952 against 3194 GB/s for the four layer
+// matrices), the two rows' x records leaving room for a shallower ring.
+bool grouped_decode_eligible(int64_t M, int64_t N, int64_t K) {
+    if (M != 1 || K % 1024 != 0 || decode_on_tensor_cores(M, K)) return false;
+    const int sms = sm_count_or_zero();
+    if (sms <= 0) return false;
+    dp::GroupArgs a{};
+    size_t smem = 0;
+    int threads = 0;
+    return dp::plan_group(1, sms, 1, &N, &K, a, smem, threads);
+}
+
+namespace {
+// The next group from problem 0 of the arrays: as many problems (at most
+// eight) as one launch's shared memory holds, with its plan; 0 when even the
+// first does not fit.
+int next_group(int G, int mt, int sms, const int64_t *N, const int64_t *K, dp::GroupArgs &a, size_t &smem,
+               int &threads) {
+    if (!dp::plan_group(mt, sms, 1, N, K, a, smem, threads)) return 0;
+    int n = 1;
+    while (n < G && n < dp::kMaxGroup) {
+        dp::GroupArgs b{};
+        size_t sm2 = 0;
+        int th2 = 0;
+        if (!dp::plan_group(mt, sms, n + 1, N, K, b, sm2, th2)) break;
+        a = b;
+        smem = sm2;
+        threads = th2;
+        ++n;
+    }
+    return n;
+}
+}  // namespace
+
+int grouped_decode_launches(int G, int64_t M, const int64_t *N, const int64_t *K) {
+    const int sms = sm_count_or_zero();
+    if (sms <= 0 || M != 1) return -1;
+    int launches = 0;
+    for (int g0 = 0; g0 < G;) {
+        dp::GroupArgs a{};
+        size_t smem = 0;
+        int threads = 0;
+        const int n = next_group(G - g0, (int)M, sms, N + g0, K + g0, a, smem, threads);
+        if (n == 0) return -1;
+        ++launches;
+        g0 += n;
+    }
+    return launches;
+}
+
+cudaError_t launch_gemv_grouped(int G, const uint16_t *const *x, const uint8_t *const *wq, float *const *y,
+                                bool ybf16, int64_t M, const int64_t *N, const int64_t *K, cudaStream_t s,
+                                unsigned int *err) {
+    const int sms = sm_count_or_zero();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    if (M != 1) return cudaErrorInvalidValue;
+    const int mt = 1;
+    for (int g0 = 0; g0 < G;) {
+        dp::GroupArgs a{};
+        size_t smem = 0;
+        int threads = 0;
+        const int n = next_group(G - g0, mt, sms, N + g0, K + g0, a, smem, threads);
+        if (n == 0) return cudaErrorInvalidValue;
+        for (int g = 0; g < n; ++g) {
+            a.it[g].x = x[g0 + g];
+            a.it[g].wq = wq[g0 + g];
+            a.it[g].y = y[g0 + g];
+        }
+        a.mrows = mt;
+        a.ybf16 = ybf16 ? 1 : 0;
+        const cudaError_t e = dp::launch_group<1>(a, smem, threads, sms, s, err);
+        if (e != cudaSuccess) return e;
+        g0 += n;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,

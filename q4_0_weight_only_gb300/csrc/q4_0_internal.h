@@ -51,6 +51,17 @@ inline float *y_offset(float *y, int64_t elems, bool ybf16) {
 // within the device limits.
 size_t gemv_workspace_bytes(int64_t M, int64_t K);
 bool gemv_shape_supported(int64_t M, int64_t N, int64_t K);
+
+// Grouped decode: independent problems y_g = x_g W_g^T with one row of x
+// each, in as few launches as shared memory allows (all of x in the CTA, one
+// weight stream).  grouped_decode_eligible: the problem can join a group
+// (M == 1, K % 1024 == 0, K <= 65536, its plan fits).  The arrays hold G eligible
+// problems; y_g has row stride N_g.
+bool grouped_decode_eligible(int64_t M, int64_t N, int64_t K);
+int grouped_decode_launches(int G, int64_t M, const int64_t *N, const int64_t *K);
+cudaError_t launch_gemv_grouped(int G, const uint16_t *const *x, const uint8_t *const *wq, float *const *y,
+                                bool ybf16, int64_t M, const int64_t *N, const int64_t *K, cudaStream_t s,
+                                unsigned int *err);
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, cudaStream_t s, unsigned int *err);
 

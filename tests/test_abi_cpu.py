@@ -116,6 +116,28 @@ def test_shapes_past_the_grid_limits_are_unsupported(lib):
     assert lib.q4_0_gemm(good, good, good, 1 << 25, 128, 256, ws, 1 << 40, None) == -2
 
 
+def test_grouped_validates_every_problem_before_any_launch(lib):
+    """q4_0_matmul_grouped checks the whole group first: a bad count, array,
+    output type or problem anywhere in it is refused before any CUDA call."""
+    P = ctypes.c_void_p
+    G = 3
+    ptrs = (P * G)(*([1 << 20] * G))
+    ns = (ctypes.c_int64 * G)(5120, 5120, 5120)
+    ks = (ctypes.c_int64 * G)(5120, 5120, 5120)
+    c = lambda a: ctypes.cast(a, P)
+    assert lib.q4_0_matmul_grouped(0, None, None, None, 0, 1, None, None, None) == 0   # nothing to do
+    assert lib.q4_0_matmul_grouped(-1, c(ptrs), c(ptrs), c(ptrs), 0, 1, c(ns), c(ks), None) == -1
+    assert lib.q4_0_matmul_grouped(G, None, c(ptrs), c(ptrs), 0, 1, c(ns), c(ks), None) == -1
+    assert lib.q4_0_matmul_grouped(G, c(ptrs), c(ptrs), c(ptrs), 0, 1, c(ns), None, None) == -1
+    assert lib.q4_0_matmul_grouped(G, c(ptrs), c(ptrs), c(ptrs), 7, 1, c(ns), c(ks), None) == -1
+    bad_k = (ctypes.c_int64 * G)(5120, 5120, 48)        # the last problem: K % 32 != 0
+    assert lib.q4_0_matmul_grouped(G, c(ptrs), c(ptrs), c(ptrs), 0, 1, c(ns), c(bad_k), None) == -1
+    misaligned = (P * G)(1 << 20, (1 << 20) + 8, 1 << 20)
+    assert lib.q4_0_matmul_grouped(G, c(misaligned), c(ptrs), c(ptrs), 0, 1, c(ns), c(ks), None) == -1
+    too_tall = (ctypes.c_int64 * G)(5120, 65535 * 128 + 1, 5120)   # tensor-core decode grid limit
+    assert lib.q4_0_matmul_grouped(G, c(ptrs), c(ptrs), c(ptrs), 0, 16, c(too_tall), c(ks), None) == -2
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     from q4_0_weight_only_gb300 import _lib
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
