@@ -356,7 +356,7 @@ def run_ours(args, rank, world, local):
                 "unit": "TFLOP/s", "frac": round(tflops / world / tf_sust, 4), "traffic": None,
                 "kernel": dominant_kernel(M), "peak_source": peak_kind + " sustained",
                 "avg_launch_us": round(ms_local * 1e3 / calls, 3)}
-    traffic = None if grouped else load_traffic(args.workload, M)
+    traffic = load_traffic("grouped" if grouped else args.workload, M)
     if traffic is not None:
         roof["traffic"] = traffic
 
