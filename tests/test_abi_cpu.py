@@ -173,3 +173,15 @@ def test_matmul_host_workspace_sizes(lib):
     assert lib.q4_0_matmul_host_workspace_bytes(1, 128, 256, 2) == 0
     assert lib.q4_0_matmul_host_workspace_bytes(0, 128, 256, 0) == 0
     assert lib.q4_0_matmul_host_workspace_bytes(1, 128, 100, 0) == 0
+
+
+def test_grouped_binding_checks_its_lists(lib):
+    """matmul_grouped: an empty group is a no-op and lists of different
+    lengths are refused before anything reaches the library."""
+    import q4_0_weight_only_gb300 as q4
+    assert q4.matmul_grouped([], [], [], []) == []
+    with pytest.raises(ValueError):
+        q4.matmul_grouped([None], [None, None], [1], [32])
+    with pytest.raises(ValueError):
+        q4.matmul_grouped([None], [None], [1], [32], outs=[None, None])
+    assert q4.grouped_launches(1, [], []) == -1
