@@ -444,6 +444,166 @@ __device__ __forceinline__ void block_dp(uint32_t dbits, const uint32_t (&Q)[4],
     }
 }
 
+// ---- pieces shared by the one-problem and the grouped kernel ----
+
+// x (MT rows of K = 64 P elements; rows >= mrows read as zero) -> the pair
+// records at xsm, by the T compute threads.  Every thread issues the loads
+// of up to kParts parts before converting any, so a CTA pays one load round
+// trip for each kParts * T parts.  Trip counts are warp-uniform.
+template <int MT>
+__device__ __forceinline__ void convert_x(const uint16_t *__restrict__ x, int64_t K, int P, int mrows,
+                                          uint32_t *__restrict__ xsm, int tid, int lane, int T) {
+    static_assert(MT <= 2, "the row of a block is blk_id >= nb");
+    constexpr int kParts = 4;
+    const int nb = 2 * P;
+    const int nparts = 2 * MT * nb;  // two threads per 32-element block
+    for (int t0 = tid - lane; t0 < nparts; t0 += kParts * T) {
+        uint4 u[kParts][2];
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) {
+            if (t0 + k * T < nparts) {
+                const int t = t0 + k * T + lane;
+                const int q = t < nparts ? t : nparts - 1;
+                const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0;
+                load_part(m < mrows ? x + (int64_t)m * K : nullptr, blk_id - m * nb, q & 1, t < nparts, u[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) {
+            if (t0 + k * T < nparts) {
+                const int t = t0 + k * T + lane;
+                const int q = t < nparts ? t : nparts - 1;
+                const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0, b = blk_id - m * nb;
+                convert_part(u[k], b, q & 1, t < nparts, xsm + ((size_t)m * P + (b >> 1)) * kPairWords);
+            }
+        }
+    }
+}
+
+// The x registers of a thread that owns block pairs tc + g * tpr (g < G).
+template <int MT>
+__device__ __forceinline__ void load_xregs(const uint32_t *__restrict__ xsm, int P, int tpr, int tc,
+                                           XReg<MT> (&xr)[Limits<MT>::kG]) {
+#pragma unroll
+    for (int g = 0; g < Limits<MT>::kG; ++g) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const uint4 *rec = reinterpret_cast<const uint4 *>(xsm + ((size_t)m * P + tc + g * tpr) * kPairWords);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 u = rec[i], w = rec[4 + i];
+                xr[g].h[m][4 * i] = u.x; xr[g].h[m][4 * i + 1] = u.y;
+                xr[g].h[m][4 * i + 2] = u.z; xr[g].h[m][4 * i + 3] = u.w;
+                xr[g].l[m][4 * i] = w.x; xr[g].l[m][4 * i + 1] = w.y;
+                xr[g].l[m][4 * i + 2] = w.z; xr[g].l[m][4 * i + 3] = w.w;
+            }
+            const uint4 t = rec[8];
+            xr[g].ncorr[m][0] = (int)t.x;
+            xr[g].ncorr[m][1] = (int)t.y;
+            xr[g].xs[m][0] = __uint_as_float(t.z);
+            xr[g].xs[m][1] = __uint_as_float(t.w);
+        }
+    }
+}
+
+// The ring of weight stages as one thread consumes it.
+struct Ring {
+    const uint8_t *smem;  // slot 0
+    uint64_t *full, *empty;
+    volatile int *abort_flag;
+    unsigned int *err;
+    int S;                // slots
+    uint32_t slot_bytes;  // bytes between slots
+};
+
+// nst stages of R whole rows (rowbytes each; the last stage last_rows rows):
+// thread (rs, tc) copies its block pairs of row rs to registers, computes,
+// then releases the stage to the producer -- only once the loaded words have
+// been used, since the next bulk fill of the slot is an async-proxy write
+// that must not overtake shared loads still in flight.  A row's pair sums
+// are reduced over kRed lanes into H partials per row at part.  The loop is
+// issue-bound at one pair per thread per stage, so the slot s, its phase ph
+// (carried across calls) and the partials' address advance incrementally:
+// a runtime division per stage cost about a tenth of the rate.  false when a
+// wait gave up.
+template <int MT>
+__device__ __forceinline__ bool stream_rows(const Ring &r, int &s, uint32_t &ph, int nst, int last_rows, int R,
+                                            int rowbytes, int H, int tpr, int tc, int rs, bool active, int lane,
+                                            const XReg<MT> (&xr)[Limits<MT>::kG], float *__restrict__ part) {
+    constexpr int G = Limits<MT>::kG, kRed = Limits<MT>::kRed;
+    const uint8_t *my_row = r.smem + (size_t)rs * rowbytes + tc * 36;
+    float *my_part = part + ((size_t)rs * H + tc / kRed) * MT;
+    const int part_step = R * H * MT;
+    for (int i = 0; i < nst; ++i) {
+        const bool ok = mbar_wait(&r.full[s], ph, r.abort_flag, r.err);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        const int rows = i == nst - 1 ? last_rows : R;
+        const bool valid = active && rs < rows;
+        uint32_t wv[G][9];
+        if (valid) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t *src =
+                    reinterpret_cast<const uint32_t *>(my_row + (uint32_t)s * r.slot_bytes + g * tpr * 36);
+#pragma unroll
+                for (int k = 0; k < 9; ++k) wv[g][k] = src[k];
+            }
+        }
+        float v[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) v[m] = 0.f;
+        if (valid) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t *w = wv[g];
+                const uint32_t Q0[4] = {__funnelshift_r(w[0], w[1], 16), __funnelshift_r(w[1], w[2], 16),
+                                        __funnelshift_r(w[2], w[3], 16), __funnelshift_r(w[3], w[4], 16)};
+                const uint32_t Q1[4] = {w[5], w[6], w[7], w[8]};
+                block_dp<MT>(w[0] & 0xFFFFu, Q0, xr[g], 0, v);
+                block_dp<MT>(w[4] >> 16, Q1, xr[g], 1, v);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.empty[s]);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float t = v[m];
+#pragma unroll
+            for (int o = kRed / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            v[m] = t;
+        }
+        if (valid && (lane & (kRed - 1)) == 0) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) my_part[m] = v[m];
+        }
+        my_part += part_step;
+        if (++s == r.S) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+    return true;
+}
+
+// Fixed-order sums over the H partials of each of a CTA's rows [r0, r1)
+// (stages of R rows), stored to y (row stride ldy); consecutive threads
+// write consecutive rows of a stage.
+template <int MT>
+__device__ __forceinline__ void row_sums(const float *__restrict__ part, int64_t r0, int64_t r1, int nst, int R,
+                                         int H, int mrows, float *__restrict__ y, int64_t ldy, bool ybf16, int tid,
+                                         int T) {
+    const int local_rows = nst * R;
+    for (int t = tid; t < local_rows * mrows; t += T) {
+        const int m = t / local_rows, lr = t - m * local_rows;
+        const int i = lr / R, rr = lr - i * R;
+        const int64_t row = r0 + (int64_t)i * R;
+        if (rr >= (int)(r1 - row < R ? r1 - row : R)) continue;
+        float sum = 0.f;
+        for (int h = 0; h < H; ++h) sum += part[((size_t)lr * H + h) * MT + m];
+        store_y(y, (int64_t)m * ldy + row + rr, sum, ybf16);
+    }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
     gemv_dp4a_kernel(const uint16_t *__restrict__ x, const uint8_t *__restrict__ wq,
@@ -529,135 +689,22 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
 
     // x -> fixed point in shared memory, once per CTA (overlaps the first copies)
     pdl_wait();
-    const int nb = 2 * a.P;
-    const int nparts = 2 * MT * nb;  // two threads per 32-element block
-    constexpr int kParts = 4;  // parts per thread per load round
-    static_assert(MT <= 2, "the row of a block is blk_id >= nb");
-    for (int t0 = tid - lane; t0 < nparts; t0 += kParts * a.T) {  // warp-uniform trip counts
-        uint4 u[kParts][2];
-#pragma unroll
-        for (int k = 0; k < kParts; ++k) {
-            if (t0 + k * a.T < nparts) {
-                const int t = t0 + k * a.T + lane;
-                const int q = t < nparts ? t : nparts - 1;
-                const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0;
-                load_part(m < a.mrows ? x + (int64_t)m * a.K : nullptr, blk_id - m * nb, q & 1, t < nparts, u[k]);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kParts; ++k) {
-            if (t0 + k * a.T < nparts) {
-                const int t = t0 + k * a.T + lane;
-                const int q = t < nparts ? t : nparts - 1;
-                const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0, b = blk_id - m * nb;
-                convert_part(u[k], b, q & 1, t < nparts, xsm + ((size_t)m * a.P + (b >> 1)) * kPairWords);
-            }
-        }
-    }
+    convert_x<MT>(x, a.K, a.P, a.mrows, xsm, tid, lane, a.T);
     named_bar_sync(1, a.T);
     if (tid == 0) mbar_arrive(xready);
 
     // thread (rs, tc) owns block pairs tc + g TPR (g < G) of row slot rs
-    constexpr int G = Limits<MT>::kG, kRed = Limits<MT>::kRed;
-    const int tpr = a.P / G;
+    const int tpr = a.P / Limits<MT>::kG;
     const int tc = tid % tpr, rs = tid / tpr;
-    const bool active = rs < a.c;
-    XReg<MT> xr[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const uint4 *rec =
-                reinterpret_cast<const uint4 *>(xsm + ((size_t)m * a.P + tc + g * tpr) * kPairWords);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 u = rec[i], w = rec[4 + i];
-                xr[g].h[m][4 * i] = u.x; xr[g].h[m][4 * i + 1] = u.y;
-                xr[g].h[m][4 * i + 2] = u.z; xr[g].h[m][4 * i + 3] = u.w;
-                xr[g].l[m][4 * i] = w.x; xr[g].l[m][4 * i + 1] = w.y;
-                xr[g].l[m][4 * i + 2] = w.z; xr[g].l[m][4 * i + 3] = w.w;
-            }
-            const uint4 t = rec[8];
-            xr[g].ncorr[m][0] = (int)t.x;
-            xr[g].ncorr[m][1] = (int)t.y;
-            xr[g].xs[m][0] = __uint_as_float(t.z);
-            xr[g].xs[m][1] = __uint_as_float(t.w);
-        }
-    }
-
-    // one row per thread per stage: copy the row's block pairs to registers,
-    // compute, then release the stage to the producer (only once the loaded
-    // words have been used: the next bulk fill of the slot is an async-proxy
-    // write and must not overtake shared loads still in flight).  The loop is
-    // issue-bound at one pair per thread per stage, so the ring slot, its
-    // phase and the partials' address advance incrementally: a runtime
-    // division per stage (i % S, i / S) cost about a tenth of the rate.
-    const int last_rows = (int)(r1 - r0 - (int64_t)(nst - 1) * a.R);
-    const uint8_t *my_row = smem + (size_t)rs * a.rowbytes + tc * 36;
-    float *my_part = part + ((size_t)rs * a.H + tc / kRed) * MT;
-    const int part_step = a.R * a.H * MT;
+    XReg<MT> xr[Limits<MT>::kG];
+    load_xregs<MT>(xsm, a.P, tpr, tc, xr);
+    const Ring ring{smem, full, empty, abort_flag, err, a.S, a.stage_bytes};
     int s = 0;
     uint32_t ph = 0;
-    for (int i = 0; i < nst; ++i) {
-        const bool ok = mbar_wait(&full[s], ph, abort_flag, err);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const int rows = i == nst - 1 ? last_rows : a.R;
-        const bool valid = active && rs < rows;
-        uint32_t wv[G][9];
-        if (valid) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const uint32_t *src =
-                    reinterpret_cast<const uint32_t *>(my_row + (uint32_t)s * a.stage_bytes + g * tpr * 36);
-#pragma unroll
-                for (int k = 0; k < 9; ++k) wv[g][k] = src[k];
-            }
-        }
-        float v[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) v[m] = 0.f;
-        if (valid) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const uint32_t *w = wv[g];
-                const uint32_t Q0[4] = {__funnelshift_r(w[0], w[1], 16), __funnelshift_r(w[1], w[2], 16),
-                                        __funnelshift_r(w[2], w[3], 16), __funnelshift_r(w[3], w[4], 16)};
-                const uint32_t Q1[4] = {w[5], w[6], w[7], w[8]};
-                block_dp<MT>(w[0] & 0xFFFFu, Q0, xr[g], 0, v);
-                block_dp<MT>(w[4] >> 16, Q1, xr[g], 1, v);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            float t = v[m];
-#pragma unroll
-            for (int o = kRed / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-            v[m] = t;
-        }
-        if (valid && (lane & (kRed - 1)) == 0) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m) my_part[m] = v[m];
-        }
-        my_part += part_step;
-        if (++s == a.S) {
-            s = 0;
-            ph ^= 1;
-        }
-    }
+    stream_rows<MT>(ring, s, ph, nst, (int)(r1 - r0 - (int64_t)(nst - 1) * a.R), a.R, a.rowbytes, a.H, tpr, tc, rs,
+                    rs < a.c, lane, xr, part);
     named_bar_sync(1, a.T);
-    // fixed-order sum over the P / 16 partials of a row; consecutive threads write
-    // consecutive rows of a stage
-    const int local_rows = nst * a.R;
-    for (int t = tid; t < local_rows * a.mrows; t += a.T) {
-        const int m = t / local_rows, lr = t - m * local_rows;
-        const int i = lr / a.R, rr = lr - i * a.R;
-        if (rr >= stage_rows(i)) continue;
-        float sum = 0.f;
-        for (int h = 0; h < a.H; ++h) sum += part[((size_t)lr * a.H + h) * MT + m];
-        store_y(y, (int64_t)m * a.ldy + stage_row0(i) + rr, sum, a.ybf16 != 0);
-    }
+    row_sums<MT>(part, r0, r1, nst, a.R, a.H, a.mrows, y, a.ldy, a.ybf16 != 0, tid, a.T);
 }
 
 struct Plan {
@@ -863,150 +910,39 @@ __global__ void __launch_bounds__(Limits<MT>::kThreads, Limits<MT>::kCtasPerSm)
 
     // x of every problem -> fixed point in its records
     pdl_wait();
-    constexpr int kParts = 4;
-    static_assert(MT <= 2, "the row of a block is blk_id >= nb");
-    for (int g = 0; g < a.G; ++g) {
-        const GroupItem &p = a.it[g];
-        uint32_t *xsm = reinterpret_cast<uint32_t *>(smem + p.off_x);
-        const int nb = 2 * p.P, nparts = 2 * MT * nb;
-        const int64_t K = (int64_t)p.P * 64;
-        for (int t0 = tid - lane; t0 < nparts; t0 += kParts * a.T) {
-            uint4 u[kParts][2];
-#pragma unroll
-            for (int k = 0; k < kParts; ++k) {
-                if (t0 + k * a.T < nparts) {
-                    const int t = t0 + k * a.T + lane;
-                    const int q = t < nparts ? t : nparts - 1;
-                    const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0;
-                    load_part(m < a.mrows ? p.x + (int64_t)m * K : nullptr, blk_id - m * nb, q & 1, t < nparts,
-                              u[k]);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kParts; ++k) {
-                if (t0 + k * a.T < nparts) {
-                    const int t = t0 + k * a.T + lane;
-                    const int q = t < nparts ? t : nparts - 1;
-                    const int blk_id = q >> 1, m = blk_id >= nb ? 1 : 0, b = blk_id - m * nb;
-                    convert_part(u[k], b, q & 1, t < nparts, xsm + ((size_t)m * p.P + (b >> 1)) * kPairWords);
-                }
-            }
-        }
-    }
+    for (int g = 0; g < a.G; ++g)
+        convert_x<MT>(a.it[g].x, (int64_t)a.it[g].P * 64, a.it[g].P, a.mrows,
+                      reinterpret_cast<uint32_t *>(smem + a.it[g].off_x), tid, lane, a.T);
     named_bar_sync(1, a.T);
     if (tid == 0) mbar_arrive(xready);
 
-    constexpr int G = Limits<MT>::kG, kRed = Limits<MT>::kRed;
+    // the problems' stages in order through one ring; the slot and its phase
+    // carry over from one problem to the next
+    const Ring ring{smem, full, empty, abort_flag, err, a.S, a.slot_bytes};
     int s = 0;
     uint32_t ph = 0;
-    bool ok = true;
-    for (int g = 0; g < a.G && ok; ++g) {
+    for (int g = 0; g < a.G; ++g) {
         const GroupItem &p = a.it[g];
         int64_t r0, r1;
         rows_of(g, r0, r1);
         const int nst = (int)((r1 - r0 + p.R - 1) / p.R);
         if (nst == 0) continue;
         // thread (rs, tc) owns block pairs tc + gg TPR of row slot rs of this problem
-        const int tpr = p.P / G;
+        const int tpr = p.P / Limits<MT>::kG;
         const int tc = tid % tpr, rs = tid / tpr;
-        const bool active = rs < p.c;
-        const uint32_t *xsm = reinterpret_cast<const uint32_t *>(smem + p.off_x);
-        XReg<MT> xr[G];
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                const uint4 *rec =
-                    reinterpret_cast<const uint4 *>(xsm + ((size_t)m * p.P + tc + gg * tpr) * kPairWords);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 u = rec[i], w = rec[4 + i];
-                    xr[gg].h[m][4 * i] = u.x; xr[gg].h[m][4 * i + 1] = u.y;
-                    xr[gg].h[m][4 * i + 2] = u.z; xr[gg].h[m][4 * i + 3] = u.w;
-                    xr[gg].l[m][4 * i] = w.x; xr[gg].l[m][4 * i + 1] = w.y;
-                    xr[gg].l[m][4 * i + 2] = w.z; xr[gg].l[m][4 * i + 3] = w.w;
-                }
-                const uint4 t = rec[8];
-                xr[gg].ncorr[m][0] = (int)t.x;
-                xr[gg].ncorr[m][1] = (int)t.y;
-                xr[gg].xs[m][0] = __uint_as_float(t.z);
-                xr[gg].xs[m][1] = __uint_as_float(t.w);
-            }
-        }
-        const int last_rows = (int)(r1 - r0 - (int64_t)(nst - 1) * p.R);
-        const uint8_t *my_row = smem + (size_t)rs * p.rowbytes + tc * 36;
-        float *my_part = reinterpret_cast<float *>(smem + p.off_part) + ((size_t)rs * p.H + tc / kRed) * MT;
-        const int part_step = p.R * p.H * MT;
-        for (int i = 0; i < nst; ++i) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag, err))) {
-                ok = false;
-                break;
-            }
-            const int rows = i == nst - 1 ? last_rows : p.R;
-            const bool valid = active && rs < rows;
-            uint32_t wv[G][9];
-            if (valid) {
-#pragma unroll
-                for (int gg = 0; gg < G; ++gg) {
-                    const uint32_t *src =
-                        reinterpret_cast<const uint32_t *>(my_row + (uint32_t)s * a.slot_bytes + gg * tpr * 36);
-#pragma unroll
-                    for (int k = 0; k < 9; ++k) wv[gg][k] = src[k];
-                }
-            }
-            float v[MT];
-#pragma unroll
-            for (int m = 0; m < MT; ++m) v[m] = 0.f;
-            if (valid) {
-#pragma unroll
-                for (int gg = 0; gg < G; ++gg) {
-                    const uint32_t *w = wv[gg];
-                    const uint32_t Q0[4] = {__funnelshift_r(w[0], w[1], 16), __funnelshift_r(w[1], w[2], 16),
-                                            __funnelshift_r(w[2], w[3], 16), __funnelshift_r(w[3], w[4], 16)};
-                    const uint32_t Q1[4] = {w[5], w[6], w[7], w[8]};
-                    block_dp<MT>(w[0] & 0xFFFFu, Q0, xr[gg], 0, v);
-                    block_dp<MT>(w[4] >> 16, Q1, xr[gg], 1, v);
-                }
-            }
-            // release the stage only once every lane has used its words
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                float t = v[m];
-#pragma unroll
-                for (int o = kRed / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                v[m] = t;
-            }
-            if (valid && (lane & (kRed - 1)) == 0) {
-#pragma unroll
-                for (int m = 0; m < MT; ++m) my_part[m] = v[m];
-            }
-            my_part += part_step;
-            if (++s == a.S) {
-                s = 0;
-                ph ^= 1;
-            }
-        }
+        XReg<MT> xr[Limits<MT>::kG];
+        load_xregs<MT>(reinterpret_cast<const uint32_t *>(smem + p.off_x), p.P, tpr, tc, xr);
+        if (!stream_rows<MT>(ring, s, ph, nst, (int)(r1 - r0 - (int64_t)(nst - 1) * p.R), p.R, p.rowbytes, p.H,
+                             tpr, tc, rs, rs < p.c, lane, xr, reinterpret_cast<float *>(smem + p.off_part)))
+            break;
     }
     named_bar_sync(1, a.T);
-    // fixed-order sums over the P / 16 partials of every row of every problem
     for (int g = 0; g < a.G; ++g) {
         const GroupItem &p = a.it[g];
         int64_t r0, r1;
         rows_of(g, r0, r1);
-        const int nst = (int)((r1 - r0 + p.R - 1) / p.R);
-        const float *part = reinterpret_cast<const float *>(smem + p.off_part);
-        const int local_rows = nst * p.R;
-        for (int t = tid; t < local_rows * a.mrows; t += a.T) {
-            const int m = t / local_rows, lr = t - m * local_rows;
-            const int i = lr / p.R, rr = lr - i * p.R;
-            const int64_t row = r0 + (int64_t)i * p.R;
-            if (rr >= (int)(r1 - row < p.R ? r1 - row : p.R)) continue;
-            float sum = 0.f;
-            for (int h = 0; h < p.H; ++h) sum += part[((size_t)lr * p.H + h) * MT + m];
-            store_y(p.y, (int64_t)m * p.N + row + rr, sum, a.ybf16 != 0);
-        }
+        row_sums<MT>(reinterpret_cast<const float *>(smem + p.off_part), r0, r1, (int)((r1 - r0 + p.R - 1) / p.R),
+                     p.R, p.H, a.mrows, p.y, p.N, a.ybf16 != 0, tid, a.T);
     }
 }
 
