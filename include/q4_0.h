@@ -19,17 +19,21 @@
  *   - weight value w = d * (q - 8).
  *
  * Conventions for every entry point below:
- *   - All array pointers are DEVICE pointers owned by the caller; the library
- *     keeps no pointer after the call returns and allocates nothing that
- *     outlives a call.
+ *   - Array pointers are DEVICE pointers owned by the caller unless an entry
+ *     point says otherwise (q4_0_matmul_host takes host x and y; the grouped
+ *     call takes host arrays of device pointers); the library keeps no
+ *     pointer after the call returns and allocates nothing that outlives a
+ *     call.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *     enqueued asynchronously on it; the caller synchronises.  Launch errors
  *     are returned; a device-side timeout is recorded in a device error word
  *     that q4_0_device_error() reads.
  *   - Arguments are validated before anything is launched; an invalid call
  *     returns a negative status and enqueues nothing.
- *   - No entry point prints, exits, or keeps host-side mutable state; calls
- *     from several host threads are safe.
+ *   - No entry point prints or exits.  The only host-side state is
+ *     process-wide caches filled once under a lock (driver entry points,
+ *     per-device kernel attributes, the fixed scratch array's address);
+ *     calls from several host threads are safe.
  *   - Results are deterministic: the same inputs give bit-identical outputs
  *     (fixed reduction order, no floating-point atomics).
  */
