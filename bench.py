@@ -46,7 +46,8 @@ def parse():
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=200)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["decode", "batched", "prefill", "sweep", "chunked"], default="decode")
+    p.add_argument("--workload", choices=["decode", "batched", "prefill", "sweep", "chunked", "chunked_split"],
+                   default="decode")
     p.add_argument("--m", type=int, default=None, help="rows of x (overrides the workload's M)")
     p.add_argument("--layers", type=int, default=8, help="resident layer copies (decode/batched)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -71,7 +72,7 @@ def workload_shapes(name, m=None):
     """M and the four layer shapes of a workload.  chunked: one 256-token
     prefill chunk and a 16-row decode batch as one M = 272 call per matrix."""
     from q4_0_weight_only_gb300 import synth
-    M = {"decode": 1, "batched": 16, "prefill": 2048, "sweep": 1, "chunked": 272}[name]
+    M = {"decode": 1, "batched": 16, "prefill": 2048, "sweep": 1, "chunked": 272, "chunked_split": 272}[name]
     if m is not None:
         M = m
     return M, [(s, synth.SHAPES[s]) for s in SHAPE_ORDER]
@@ -215,8 +216,11 @@ def run_ours(args, rank, world, local):
     ydt = torch.bfloat16 if args.y_dtype == "bf16" else torch.float32
     ysz = 2 if args.y_dtype == "bf16" else 4
     ys = [torch.empty((M, N), dtype=ydt, device=dev) for _, (N, K) in shapes]
-    wss = [torch.empty(max(1, q4.lib().q4_0_matmul_workspace_bytes(M, N, K)), dtype=torch.uint8,
-                       device=dev) for _, (N, K) in shapes]
+    # row ranges of x issued as separate calls: chunked_split runs the
+    # 256-token chunk and the 16 decode rows of each matrix as two calls
+    parts = [(0, 256), (256, M)] if args.workload == "chunked_split" else [(0, M)]
+    wss = [[torch.empty(max(1, q4.lib().q4_0_matmul_workspace_bytes(m1 - m0, N, K)), dtype=torch.uint8,
+                        device=dev) for m0, m1 in parts] for _, (N, K) in shapes]
     stream = torch.cuda.Stream(device=dev)
 
     sweep = args.workload == "sweep"
@@ -238,7 +242,9 @@ def run_ours(args, rank, world, local):
                 q4.matmul_grouped(xs, wq[l], Ns, Ks, outs=ys, stream=stream, out_dtype=ydt)
                 continue
             for j, (_, (N, K)) in enumerate(shapes):
-                q4.matmul(xs[j], wq[l][j], N, K, out=ys[j], workspace=wss[j], stream=stream, out_dtype=ydt)
+                for p, (m0, m1) in enumerate(parts):
+                    q4.matmul(xs[j][m0:m1], wq[l][j], N, K, out=ys[j][m0:m1], workspace=wss[j][p], stream=stream,
+                              out_dtype=ydt)
 
     # CUDA graphs: one graph per full cycle of the resident layer copies (a
     # decode engine captures a whole pass the same way), plus one graph per
@@ -258,11 +264,12 @@ def run_ours(args, rank, world, local):
         with torch.cuda.graph(full, stream=stream):
             for v in range(cycle):
                 enqueue_step(v)
-    calls_per_step = len(shapes) * (layers if sweep else 1)
+    calls_per_step = len(shapes) * len(parts) * (layers if sweep else 1)
     if grouped:
         launches_per_step = q4.grouped_launches(M, Ns, Ks) * (layers if sweep else 1)
     else:
-        launches_per_step = sum(kernels_per_call(q4, M, N, K) for _, (N, K) in shapes) * (layers if sweep else 1)
+        launches_per_step = sum(kernels_per_call(q4, m1 - m0, N, K) for _, (N, K) in shapes
+                                for m0, m1 in parts) * (layers if sweep else 1)
 
     def run_steps(n):
         for _ in range(n // cycle):
@@ -310,8 +317,8 @@ def run_ours(args, rank, world, local):
     # page-locked host memory (read and written in place by the kernels
     # where the device maps it, else copied); its device scratch holds the
     # rest
-    whs = [torch.empty(q4.host_workspace_bytes(M, N, K, ydt), dtype=torch.uint8, device=dev)
-           for _, (N, K) in shapes]
+    whs = [[torch.empty(q4.host_workspace_bytes(m1 - m0, N, K, ydt), dtype=torch.uint8, device=dev)
+            for m0, m1 in parts] for _, (N, K) in shapes]
     h2d = sum(x.numel() * 2 for x in x_host) * (layers if sweep else 1)
     d2h = sum(y.numel() * ysz for y in y_host) * (layers if sweep else 1)
     torch.cuda.synchronize()
@@ -331,8 +338,9 @@ def run_ours(args, rank, world, local):
                         y_host[j].copy_(ys[j], non_blocking=True)
                     continue
                 for j, (_, (N, K)) in enumerate(shapes):
-                    q4.matmul_host(x_host[j], wq[l][j], N, K, out=y_host[j], workspace=whs[j], stream=stream,
-                                   out_dtype=ydt)
+                    for p, (m0, m1) in enumerate(parts):
+                        q4.matmul_host(x_host[j][m0:m1], wq[l][j], N, K, out=y_host[j][m0:m1], workspace=whs[j][p],
+                                       stream=stream, out_dtype=ydt)
             stream.synchronize()
     t_e2e = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
@@ -395,6 +403,8 @@ def workload_name(w, M, layers, grouped=False):
             "batched": f"batched decode M={M}, four 27B-class layer matrices per step, {layers} layer copies",
             "prefill": f"prefill M={M}, four 27B-class layer matrices per step",
             "sweep": f"64-layer decode sweep at M={M} (256 matrices per step)",
+            "chunked_split": f"chunked prefill: 256-token chunk + 16 decode rows as two calls per matrix "
+                             f"(M=256 and M={M - 256}), four matrices per step, {layers} layer copies",
             "chunked": f"chunked prefill: 256-token chunk + 16 decode rows as one M={M} call per matrix, "
                        f"four matrices per step, {layers} layer copies"}[w]
 
