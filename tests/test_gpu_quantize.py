@@ -59,3 +59,16 @@ def test_edge_blocks_bit_exact():
         assert np.array_equal(gpu_quantize(sub), oracle.get().quantize(sub))
     wide = w[: (w.shape[0] // 8) * 8].reshape(-1, 256)
     assert np.array_equal(gpu_quantize(wide), oracle.get().quantize(wide))
+
+
+@pytest.mark.parametrize("layer", [0, 63])
+def test_sweep_layers_bit_exact(layer):
+    """The 64-layer sweep draws its weights on the device and quantizes them
+    there; its first and last layers, all four shapes, match the oracle's
+    quantizer on the same values bit for bit."""
+    q4 = lib()
+    for shape in synth.SHAPE_ORDER:
+        w = synth.device_layer_weights(layer, shape)
+        got = q4.quantize(w).cpu().numpy()
+        assert np.array_equal(got, oracle.get().quantize(w.cpu().numpy())), shape
+        del w
