@@ -46,6 +46,13 @@
 #endif
 
 #define ORACLE_QK 32          /* weights per block */
+
+/* The scale's bits from the first two bytes of a block (little-endian). */
+#if ORACLE_MUTANT == 10
+#define ORACLE_D_BITS(blk) ((uint16_t)((blk)[1] | ((blk)[0] << 8))) /* mutant: scale bytes swapped */
+#else
+#define ORACLE_D_BITS(blk) ((uint16_t)((blk)[0] | ((blk)[1] << 8)))
+#endif
 #define ORACLE_BLOCK_BYTES 18 /* 2 bytes of d + 16 bytes of codes */
 
 /* ---------------------------------------------------------------- binary16 */
@@ -159,12 +166,21 @@ static void oracle_quantize_block(const float *w, uint8_t *out) {
             float r = w[j] / d;
             int c = (int)oracle_round_half_away(r) + 8;
             if (c < 0) c = 0;
+#if ORACLE_MUTANT == 11
+            if (c > 14) c = 14; /* mutant: codes clamped one short of 15 */
+#else
             if (c > 15) c = 15;
+#endif
             q[j] = (uint8_t)c;
         }
     }
+#if ORACLE_MUTANT == 10
+    out[0] = (uint8_t)(dbits >> 8); /* mutant: scale bytes swapped */
+    out[1] = (uint8_t)(dbits & 0xFFu);
+#else
     out[0] = (uint8_t)(dbits & 0xFFu);
     out[1] = (uint8_t)(dbits >> 8);
+#endif
     for (int j = 0; j < 16; ++j) {
 #if ORACLE_MUTANT == 1
         out[2 + j] = (uint8_t)((q[j] << 4) | q[j + 16]); /* mutant: nibbles swapped */
@@ -192,7 +208,7 @@ void oracle_unpack(const uint8_t *wq, uint8_t *codes, uint16_t *dbits, int64_t N
     for (int64_t n = 0; n < N; ++n)
         for (int64_t b = 0; b < nb; ++b) {
             const uint8_t *blk = wq + (n * nb + b) * ORACLE_BLOCK_BYTES;
-            dbits[n * nb + b] = (uint16_t)(blk[0] | (blk[1] << 8));
+            dbits[n * nb + b] = ORACLE_D_BITS(blk);
             uint8_t *c = codes + n * K + b * ORACLE_QK;
             for (int j = 0; j < 16; ++j) {
 #if ORACLE_MUTANT == 1
@@ -211,7 +227,7 @@ static void oracle_decode_row(const uint8_t *wq, int64_t n, int64_t K, double *r
     int64_t nb = K / ORACLE_QK;
     for (int64_t b = 0; b < nb; ++b) {
         const uint8_t *blk = wq + (n * nb + b) * ORACLE_BLOCK_BYTES;
-        double d = oracle_f16_bits_to_f64((uint16_t)(blk[0] | (blk[1] << 8)));
+        double d = oracle_f16_bits_to_f64(ORACLE_D_BITS(blk));
         for (int j = 0; j < 16; ++j) {
 #if ORACLE_MUTANT == 1
             int lo = blk[2 + j] >> 4, hi = blk[2 + j] & 15;
