@@ -71,7 +71,7 @@ def peaks():
 def workload_shapes(name, m=None):
     """M and the four layer shapes of a workload.  chunked: one 256-token
     prefill chunk and a 16-row decode batch as one M = 272 call per matrix."""
-    from q4_0_weight_only_gb300 import synth
+    from q4_weight_only_gb300 import synth
     M = {"decode": 1, "batched": 16, "prefill": 2048, "sweep": 1, "chunked": 272, "chunked_split": 272}[name]
     if m is not None:
         M = m
@@ -199,10 +199,10 @@ def build_layers(q4, synth, shapes, layers, device):
 
 def run_ours(args, rank, world, local):
     import torch
-    from q4_0_weight_only_gb300 import build as lib_build
+    from q4_weight_only_gb300 import build as lib_build
     lib_build.build()
-    import q4_0_weight_only_gb300 as q4
-    from q4_0_weight_only_gb300 import synth
+    import q4_weight_only_gb300 as q4
+    from q4_weight_only_gb300 import synth
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -484,7 +484,7 @@ def run_reference(args, rank, world, local):
     if rank != 0:
         return None
     import oracle
-    from q4_0_weight_only_gb300 import synth
+    from q4_weight_only_gb300 import synth
     o = oracle.get()
     M, shapes = workload_shapes(args.workload, args.m)
     warm = max(3, args.warmup)

@@ -2,7 +2,7 @@
 
 The compute lives in libq4_0.so (hand-written CUDA: a decode GEMV, a tcgen05
 tensor-core GEMM and a quantizer); this package is its thin Python binding.
-Build it with ``q4_0_weight_only_gb300.build.build()``.
+Build it with ``q4_weight_only_gb300.build.build()``.
 """
 from ._lib import (ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_INVALID_ARG, ERR_UNSUPPORTED,
                    ERR_WORKSPACE, OK, Y_BF16, Y_F32, Q4Error, device_error, gemm, gemv, gemv_alloc, lib, matmul,

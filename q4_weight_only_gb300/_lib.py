@@ -66,7 +66,7 @@ def lib():
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with q4_0_weight_only_gb300.build.build() "
+                f"{LIB_PATH} is missing: build it with q4_weight_only_gb300.build.build() "
                 "(nvcc, sm_103a). There is no fallback implementation.")
         l = ctypes.CDLL(LIB_PATH)
         for name, (args, res) in SIGNATURES.items():

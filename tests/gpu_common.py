@@ -7,9 +7,9 @@ import oracle
 
 
 def lib():
-    from q4_0_weight_only_gb300 import build
+    from q4_weight_only_gb300 import build
     build.build()
-    import q4_0_weight_only_gb300 as q4
+    import q4_weight_only_gb300 as q4
     return q4
 
 

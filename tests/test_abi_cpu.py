@@ -19,7 +19,7 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def lib():
-    from q4_0_weight_only_gb300 import build, _lib
+    from q4_weight_only_gb300 import build, _lib
     build.build()
     return _lib.lib()
 
@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
 
 
 def test_every_declared_symbol_is_exported(lib):
-    from q4_0_weight_only_gb300 import _lib
+    from q4_weight_only_gb300 import _lib
     names = declared_functions()
     for n in names:
         assert hasattr(lib, n), n
@@ -139,7 +139,7 @@ def test_grouped_validates_every_problem_before_any_launch(lib):
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
-    from q4_0_weight_only_gb300 import _lib
+    from q4_weight_only_gb300 import _lib
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError):
@@ -178,7 +178,7 @@ def test_matmul_host_workspace_sizes(lib):
 def test_grouped_binding_checks_its_lists(lib):
     """matmul_grouped: an empty group is a no-op and lists of different
     lengths are refused before anything reaches the library."""
-    import q4_0_weight_only_gb300 as q4
+    import q4_weight_only_gb300 as q4
     assert q4.matmul_grouped([], [], [], []) == []
     with pytest.raises(ValueError):
         q4.matmul_grouped([None], [None, None], [1], [32])

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from gpu_common import check_full, lib, wq_dev, x_dev
-from q4_0_weight_only_gb300 import synth
+from q4_weight_only_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from gpu_common import check_sampled, lib
-from q4_0_weight_only_gb300 import synth
+from q4_weight_only_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from gpu_common import check_full, check_sampled, lib, wq_dev, x_dev
-from q4_0_weight_only_gb300 import synth
+from q4_weight_only_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 

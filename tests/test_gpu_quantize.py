@@ -6,7 +6,7 @@ import torch
 import oracle
 import pins
 from gpu_common import lib
-from q4_0_weight_only_gb300 import synth
+from q4_weight_only_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
