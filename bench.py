@@ -56,6 +56,8 @@ def parse():
                    help="decode (M = 1): each layer's matrices as one q4_0_matmul_grouped call")
     p.add_argument("--y-dtype", choices=["f32", "bf16"], default="f32",
                    help="element type of y (bf16: the rounded-once output of q4_0_matmul_ex)")
+    p.add_argument("--no-sub", action="store_true",
+                   help="decode: skip the batched / prefill / chunked results beside the headline")
     return p.parse_args()
 
 
@@ -197,19 +199,22 @@ def build_layers(q4, synth, shapes, layers, device):
     return wq
 
 
-def run_ours(args, rank, world, local):
-    import torch
-    from q4_weight_only_gb300 import build as lib_build
-    lib_build.build()
-    import q4_weight_only_gb300 as q4
-    from q4_weight_only_gb300 import synth
+# Spin kernel run just before the start event: the device stays busy while
+# the host enqueues the start event and the timed graph replays, so the timed
+# region holds the K steps back to back and no host submission latency.
+BUSY_CYCLES = 2_000_000
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+
+def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=False):
+    """Time `args.steps` steps of one workload on the resident layer copies
+    `wq` (a list of per-layer lists of the four Q4_0 matrices) and return the
+    workload's result: value, roofline of the dominant kernel, e2e through
+    the host-buffer entry point, clocks and launch counts."""
+    import torch
     hbm, tf_burst, tf_sust, peak_kind = peaks()
-    M, shapes = workload_shapes(args.workload, args.m)
-    layers = 64 if args.workload == "sweep" else (1 if args.workload == "prefill" else args.layers)
-    wq = build_layers(q4, synth, shapes, layers, dev)
+    shapes = [(s, synth.SHAPES[s]) for s in SHAPE_ORDER]
+    sweep = workload == "sweep"
+    layers = len(wq)
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     xs = [torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16) for _, (N, K) in shapes]
@@ -218,22 +223,17 @@ def run_ours(args, rank, world, local):
     ys = [torch.empty((M, N), dtype=ydt, device=dev) for _, (N, K) in shapes]
     # row ranges of x issued as separate calls: chunked_split runs the
     # 256-token chunk and the 16 decode rows of each matrix as two calls
-    parts = [(0, 256), (256, M)] if args.workload == "chunked_split" else [(0, M)]
+    parts = [(0, 256), (256, M)] if workload == "chunked_split" else [(0, M)]
     wss = [[torch.empty(max(1, q4.lib().q4_0_matmul_workspace_bytes(m1 - m0, N, K)), dtype=torch.uint8,
                         device=dev) for m0, m1 in parts] for _, (N, K) in shapes]
     stream = torch.cuda.Stream(device=dev)
 
-    sweep = args.workload == "sweep"
     per_step_layers = layers if sweep else 1  # a sweep step passes through every layer
     step_bytes = per_step_layers * sum(alg_bytes(M, N, K, ysz) for _, (N, K) in shapes)
     step_flops = per_step_layers * sum(2.0 * M * N * K for _, (N, K) in shapes)
     step_weights = per_step_layers * sum(N * K for _, (N, K) in shapes)
-
     Ns = [N for _, (N, K) in shapes]
     Ks = [K for _, (N, K) in shapes]
-    grouped = args.grouped and q4.grouped_launches(M, Ns, Ks) > 0
-    if args.grouped and not grouped:
-        raise SystemExit("--grouped: the grouped decode does not take these shapes at this M")
 
     def enqueue_step(i):
         ls = range(layers) if sweep else (i % layers,)
@@ -246,24 +246,6 @@ def run_ours(args, rank, world, local):
                     q4.matmul(xs[j][m0:m1], wq[l][j], N, K, out=ys[j][m0:m1], workspace=wss[j][p], stream=stream,
                               out_dtype=ydt)
 
-    # CUDA graphs: one graph per full cycle of the resident layer copies (a
-    # decode engine captures a whole pass the same way), plus one graph per
-    # single step for a remainder, so that exactly `steps` steps run
-    cycle = 1 if sweep else layers
-    single = []
-    with torch.cuda.stream(stream):
-        for i in range(3):  # load/initialise before capture
-            enqueue_step(i)
-        stream.synchronize()
-        for v in range(cycle):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
-                enqueue_step(v)
-            single.append(gr)
-        full = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(full, stream=stream):
-            for v in range(cycle):
-                enqueue_step(v)
     calls_per_step = len(shapes) * len(parts) * (layers if sweep else 1)
     if grouped:
         launches_per_step = q4.grouped_launches(M, Ns, Ks) * (layers if sweep else 1)
@@ -271,17 +253,51 @@ def run_ours(args, rank, world, local):
         launches_per_step = sum(kernels_per_call(q4, m1 - m0, N, K) for _, (N, K) in shapes
                                 for m0, m1 in parts) * (layers if sweep else 1)
 
-    def run_steps(n):
-        for _ in range(n // cycle):
-            full.replay()
-        for v in range(n % cycle):
-            single[v].replay()
+    # CUDA graphs (a decode engine captures a whole pass the same way): the
+    # timed steps as one graph when they fit about a thousand kernels,
+    # otherwise a graph of a whole number of layer cycles replayed, plus one
+    # graph for the remainder.  Step i of a graph uses layer copy i mod the
+    # copies, and every graph but the last holds whole cycles, so the copies
+    # rotate without a break across replays.
+    cycle = 1 if sweep else layers
+    max_steps_per_graph = max(1, 1024 // max(1, launches_per_step))
 
-    warm = max(3, args.warmup)
+    def capture(n):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for v in range(n):
+                enqueue_step(v)
+        return gr
+
     with torch.cuda.stream(stream):
-        run_steps(warm)
+        for i in range(3):  # load/initialise before capture
+            enqueue_step(i)
+        stream.synchronize()
+        if args.steps <= max_steps_per_graph:
+            plan = [(capture(args.steps), args.steps, 1)]
+        else:
+            C = max(cycle, max_steps_per_graph // cycle * cycle)
+            reps, rem = divmod(args.steps, C)
+            plan = [(capture(C), C, reps)] + ([(capture(rem), rem, 1)] if rem else [])
+
+    def run_timed():
+        for gr, _, reps in plan:
+            for _ in range(reps):
+                gr.replay()
+
+    # warm-up: every graph replays at least once before the timed region
+    # (a graph's first replay uploads it), then at least the requested
+    # warm-up steps
+    warm = 0
+    with torch.cuda.stream(stream):
+        for gr, n, _ in plan:
+            gr.replay()
+            warm += n
+        while warm < max(3, args.warmup):
+            plan[0][0].replay()
+            warm += plan[0][1]
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
@@ -289,10 +305,18 @@ def run_ours(args, rank, world, local):
     ev1 = torch.cuda.Event(enable_timing=True)
     clocks.mark_start()
     with torch.cuda.stream(stream):
+        torch.cuda._sleep(BUSY_CYCLES)
         ev0.record(stream)
-        run_steps(args.steps)
+        run_timed()
         ev1.record(stream)
     ev1.synchronize()
+    # keep the clock sampler's window on the work for short regions
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if elapsed < 0.5:
+        with torch.cuda.stream(stream):
+            for _ in range(int(0.5 / max(elapsed, 1e-6)) + 1):
+                run_timed()
+        stream.synchronize()
     clocks.mark_end()
     torch.cuda.synchronize()
     barrier(world)
@@ -321,76 +345,140 @@ def run_ours(args, rank, world, local):
             for m0, m1 in parts] for _, (N, K) in shapes]
     h2d = sum(x.numel() * 2 for x in x_host) * (layers if sweep else 1)
     d2h = sum(y.numel() * ysz for y in y_host) * (layers if sweep else 1)
+
+    def e2e_step(i):
+        ls = range(layers) if sweep else (i % layers,)
+        for l in ls:
+            if grouped:
+                # the grouped call takes device buffers: x copied in and y
+                # copied out around it, on the same stream
+                for j in range(len(shapes)):
+                    xs[j].copy_(x_host[j], non_blocking=True)
+                q4.matmul_grouped(xs, wq[l], Ns, Ks, outs=ys, stream=stream, out_dtype=ydt)
+                for j in range(len(shapes)):
+                    y_host[j].copy_(ys[j], non_blocking=True)
+                continue
+            for j, (_, (N, K)) in enumerate(shapes):
+                for p, (m0, m1) in enumerate(parts):
+                    q4.matmul_host(x_host[j][m0:m1], wq[l][j], N, K, out=y_host[j][m0:m1], workspace=whs[j][p],
+                                   stream=stream, out_dtype=ydt)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(min(3, e2e_steps)):  # first calls of the host path outside the timing
+            e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(e2e_steps):
-            ls = range(layers) if sweep else (i % layers,)
-            for l in ls:
-                if grouped:
-                    # the grouped call takes device buffers: x copied in and
-                    # y copied out around it, on the same stream
-                    for j in range(len(shapes)):
-                        xs[j].copy_(x_host[j], non_blocking=True)
-                    q4.matmul_grouped(xs, wq[l], Ns, Ks, outs=ys, stream=stream, out_dtype=ydt)
-                    for j in range(len(shapes)):
-                        y_host[j].copy_(ys[j], non_blocking=True)
-                    continue
-                for j, (_, (N, K)) in enumerate(shapes):
-                    for p, (m0, m1) in enumerate(parts):
-                        q4.matmul_host(x_host[j][m0:m1], wq[l][j], N, K, out=y_host[j][m0:m1], workspace=whs[j][p],
-                                       stream=stream, out_dtype=ydt)
-            stream.synchronize()
+            e2e_step(i)
     t_e2e = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
-    e2e_val = (step_bytes if M < 256 else step_flops) * e2e_steps * world / t_e2e / (1e9 if M < 256 else 1e12)
+    tensor_bound = M >= 256
+    e2e_val = (step_flops if tensor_bound else step_bytes) * e2e_steps * world / t_e2e / (1e12 if tensor_bound else 1e9)
 
-    unit = "GB/s" if M < 256 else "TFLOP/s"
-    value = gbs if M < 256 else tflops
-    # roofline of the dominant kernel (the only kernel in the timed region)
+    unit = "TFLOP/s" if tensor_bound else "GB/s"
+    value = tflops if tensor_bound else gbs
     launches = args.steps * launches_per_step
     if grouped:
         calls_per_step = launches_per_step  # one grouped launch covers several matmuls
     calls = args.steps * calls_per_step  # launches of the dominant kernel (one per matmul)
-    if M < 256:
+    if not tensor_bound:
         roof = {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(gbs / world / hbm, 4), "traffic": None,
-                "kernel": dominant_kernel(M, grouped), "peak_source": peak_kind,
+                "kernel": dominant_kernel(M, grouped), "peak_source": peak_kind + " (copy bandwidth)",
                 "bytes_per_launch": round(step_bytes / calls_per_step),
-                "avg_launch_us": round(ms_local * 1e3 / calls, 3)}
+                "avg_launch_us": round(ms_local * 1e3 / calls, 3),
+                "timing": "whole step on the launching stream (every kernel of the step), / matmul calls"}
     else:
-        roof = {"bound": "tensor", "achieved": round(tflops / world, 1), "peak": tf_sust,
-                "unit": "TFLOP/s", "frac": round(tflops / world / tf_sust, 4), "traffic": None,
-                "kernel": dominant_kernel(M), "peak_source": peak_kind + " sustained",
-                "avg_launch_us": round(ms_local * 1e3 / calls, 3)}
-    traffic = load_traffic("grouped" if grouped else args.workload, M)
+        # a GEMM timed inside a short region: the burst peak; the sustained
+        # fraction beside it
+        roof = {"bound": "tensor", "achieved": round(tflops / world, 1), "peak": tf_burst,
+                "unit": "TFLOP/s", "frac": round(tflops / world / tf_burst, 4), "traffic": None,
+                "kernel": dominant_kernel(M), "peak_source": peak_kind + " bf16 burst (kind::f16 runs at the bf16 rate)",
+                "frac_of_sustained": round(tflops / world / tf_sust, 4), "peak_sustained": tf_sust,
+                "flops_per_launch": round(step_flops / calls_per_step),
+                "avg_launch_us": round(ms_local * 1e3 / calls, 3),
+                "timing": "whole step on the launching stream (x pre-pass and split-K sum included), / matmul calls"}
+    traffic = load_traffic("grouped" if grouped else workload, M)
     if traffic is not None:
         roof["traffic"] = traffic
+    res = {"workload": workload_name(workload, M, layers, grouped), "M": M,
+           "value": round(value, 2), "unit": unit, "steps": args.steps, "warmup": warm,
+           "ms_per_step": round(ms / args.steps, 5),
+           "tok_s_eq": round(tok_s, 1), "tflops": round(tflops, 2), "gbs": round(gbs, 1),
+           "gpu_launches": launches, "roofline": roof, "clocks": clk,
+           "e2e": {"value": round(e2e_val, 2), "unit": unit, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+           "layer_copies": layers,
+           "graphs": " + ".join(f"{reps} x {n} steps" for _, n, reps in plan)}
+    if cpu:
+        res["cpu_baseline"] = cpu_baseline(wq[0], xs, shapes, M, budget_s=10.0)
+    del xs, ys, wss, whs, plan
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
+
+# The default run reports these beside the decode headline: the other parts
+# of the metric (batched decode, prefill TFLOP/s, chunked prefill) on the
+# same resident layer copies.
+SUB_WORKLOADS = (("batched_m16", "batched", 16), ("prefill_m2048", "prefill", 2048),
+                 ("chunked_m272", "chunked", 272))
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from q4_weight_only_gb300 import build as lib_build
+    lib_build.build()
+    import q4_weight_only_gb300 as q4
+    from q4_weight_only_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    M, shapes = workload_shapes(args.workload, args.m)
+    layers = 64 if args.workload == "sweep" else (1 if args.workload == "prefill" else args.layers)
+    wq = build_layers(q4, synth, shapes, layers, dev)
+    Ns = [N for _, (N, K) in shapes]
+    Ks = [K for _, (N, K) in shapes]
+    grouped = args.grouped and q4.grouped_launches(M, Ns, Ks) > 0
+    if args.grouped and not grouped:
+        raise SystemExit("--grouped: the grouped decode does not take these shapes at this M")
+    cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    head = measure(q4, synth, wq, args.workload, M, args, dev, world, grouped=grouped, cpu=cpu)
+
+    subs = {}
+    if args.workload == "decode" and args.m is None and not grouped and not args.no_sub:
+        for key, wl, m in SUB_WORKLOADS:
+            subs[key] = measure(q4, synth, wq[:1] if wl == "prefill" else wq, wl, m, args, dev, world)
+
+    dt = ("q4_0 codes x 15-bit fixed-point x: int dp4a in-block, f32 across blocks" if M <= 2 else
+          "q4_0 weights -> f16 tiles; f16 MMA, f32 accumulate")
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": warm, "ms_per_step": round(ms / args.steps, 5),
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": head["warmup"], "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("q4_0 codes x 15-bit fixed-point x: int dp4a in-block, f32 across blocks" if M <= 2 else
-                  "q4_0 weights -> f16 tiles; f16 MMA, f32 accumulate"),
+        "dtype": dt,
         "data": "synthetic: W ~ N(0, 0.02) quantized on device, x ~ N(0, 1) bf16",
-        "config": {"workload": workload_name(args.workload, M, layers, grouped), "M": M,
+        "config": {"workload": head["workload"], "M": M,
                    "shapes": {s: list(nk) for s, nk in shapes}, "layer_copies": layers,
                    "l2": "inputs larger than L2: %d resident layer copies, %.2f GB cycled"
                          % (layers, layers * sum(0.5625 * N * K for _, (N, K) in shapes) / 1e9),
                    "y": args.y_dtype, "parallelism": f"replicas x{world}",
-                   "graph": f"one CUDA graph per {cycle} step(s), replayed; PDL between kernels"},
-        "tok_s_eq": round(tok_s, 1),
-        "tflops": round(tflops, 2),
-        "gpu_launches": launches,
-        "roofline": roof,
-        "clocks": clk,
-        "e2e": {"value": round(e2e_val, 2), "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                   "graph": f"timed steps as CUDA graph replays ({head['graphs']}); PDL between kernels; "
+                            "a spin kernel keeps the device busy across the start event"},
+        "tok_s_eq": head["tok_s_eq"],
+        "tflops": head["tflops"],
+        "gpu_launches": head["gpu_launches"],
+        "roofline": head["roofline"],
+        "clocks": head["clocks"],
+        "e2e": head["e2e"],
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wq[0], xs, shapes, M, budget_s=10.0)
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if subs:
+        line["sub"] = subs
     return line if rank == 0 else None
 
 
@@ -417,7 +505,7 @@ def kernels_per_call(q4, M, N, K):
         return 1
     if M <= 32:
         return 2
-    x16 = (M * K * 2 + 255) // 256 * 256
+    x16 = (M * K * 2 + 255) // 256 * 256 + (M * 4 + 255) // 256 * 256  # x as binary16 and its row scales
     return 3 if q4.lib().q4_0_gemm_workspace_bytes(M, N, K) > x16 else 2
 
 

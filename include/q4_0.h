@@ -23,7 +23,10 @@
  *     point says otherwise (q4_0_matmul_host takes host x and y; the grouped
  *     call takes host arrays of device pointers); the library keeps no
  *     pointer after the call returns and allocates nothing that outlives a
- *     call.
+ *     call.  The one exception is the fixed scratch array of
+ *     q4_0_gemm_noalloc (Q4_0_NOALLOC_SCRATCH_BYTES of device memory),
+ *     which is reserved when the library is loaded on a device and held
+ *     until the process exits.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *     enqueued asynchronously on it; the caller synchronises.  Launch errors
  *     are returned; a device-side timeout is recorded in a device error word
@@ -107,10 +110,34 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
  * K > 65536 (x no longer fits shared memory), run the batched decode on the
  * tensor cores; M > 32 runs the tcgen05 GEMM (weights dequantised to
  * binary16 tiles, x rounded to binary16, fp32 accumulation in tensor
- * memory).  All meet: per element
- * |y - y_exact| <= 1e-2 * sum_k |w x| and relative L2 error <= 2e-3.
- * Activations must be finite with |x| <= 65504 (the tensor-core paths round
- * x to binary16).
+ * memory).
+ * Accuracy.  Inputs must be finite and y must stay within the fp32 range;
+ * the tensor-core paths also need |w| = |d (q - 8)| <= 65504.
+ * Every path accumulates in fp32 and differs from the exact sum only in the
+ * form it gives w and x:
+ *   - tensor-core paths (3 <= M, or M <= 2 with K > 65536): each weight
+ *     rounded once to binary16 (relative error <= 2^-11); each row of x
+ *     scaled by a power of two (its largest |x| to [2^14, 2^15), undone
+ *     exactly at the store) and rounded to binary16: exact for every
+ *     element within 2^29 of the row's largest |x|, absolute error
+ *     <= 2^-39 times that largest |x| below;
+ *   - integer-dot decode (M <= 2, K % 1024 == 0, K <= 65536): weights
+ *     exact; x in 15-bit fixed point per 32-element block, absolute error
+ *     <= 2^-14 B per element, B the largest |x| of its block;
+ *   - binary16 decode (M <= 2, other K <= 65536): weights exact; x in
+ *     binary16 scaled per 32-element block, absolute error <= 2^-24 B.
+ * Per element, |y - y_exact| <= 1e-2 * sum_k |w x| then holds on the
+ * tensor-core paths for every x whose rows span at most 2^29, on the
+ * binary16 decode whenever sum_k |w| B <= 2^17 sum_k |w x|, and on the
+ * integer-dot decode whenever sum_k |w| B <= 150 sum_k |w x| (with B of the
+ * element's block; for N(0, 1) activations the ratio is about 3, with 1 %
+ * of them 20x larger about 7).  Outside that condition the integer-dot
+ * decode's error stays within 2^-14 sum_k |w| B plus fp32 rounding: one
+ * element per block far above the others (a block of x spanning 2^15) with
+ * its weight near zero is the case it does not cover.  The relative L2
+ * error ||y - y_exact|| / ||y_exact|| is at most 2e-3 on the workloads' data
+ * on every path (it is relative to ||y||, which cancellation can make
+ * arbitrarily small, so it is a measured property, not a per-input bound).
  * Scratch: the tensor-core decode and GEMM (M > 32) paths need
  * q4_0_matmul_workspace_bytes(M, N, K) bytes; this entry point takes them
  * with cudaMallocAsync on `stream` and frees them with cudaFreeAsync on the
@@ -268,7 +295,13 @@ int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y,
  * this entry point exists for callers where the CUDA allocator must not be
  * entered (host callbacks, real-time loops with no allocation after
  * start-up, plug-ins whose host owns every device byte).
- *   x, wq, y, M, N, K, stream : as in q4_0_gemm (same kernels, same result).
+ *   x, wq, y, M, N, K, stream : as in q4_0_gemm, and the same kernels run,
+ *   with one difference: this entry point never splits K over several CTAs
+ *   (the array holds the binary16 copy of x only).  q4_0_gemm splits K when
+ *   the output tiles alone leave SMs idle, and a split sums in another
+ *   order, so the two results can differ in the last bits (both meet the
+ *   result contract of q4_0_matmul), and for few output tiles this entry
+ *   point keeps fewer SMs busy.
  * Scratch: a fixed array of Q4_0_NOALLOC_SCRATCH_BYTES in device memory,
  * reserved when the library is loaded on a GPU and held until the process
  * exits; nothing is allocated or freed per call.  It fits M * K * 2 bytes,

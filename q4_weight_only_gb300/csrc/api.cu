@@ -93,14 +93,15 @@ unsigned int *device_error_word() {
 using namespace q4_0;
 
 namespace {
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
 
+namespace q4_0 {
 // Common validation of a matmul call.
 // `any_k`: K % 32 == 0 is enough (the dispatcher pads other K to a multiple
 // of 256); the kernel-alone entry points need K % 256 == 0.
 int check_matmul_args(const void *x, const void *wq, const void *y, int64_t M, int64_t N,
-                      int64_t K, bool any_k = false) {
+                      int64_t K, bool any_k) {
     if (!x || !wq || !y) return Q4_0_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return Q4_0_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(wq) || !aligned16(y)) return Q4_0_ERR_INVALID_ARG;
@@ -111,6 +112,9 @@ int check_matmul_args(const void *x, const void *wq, const void *y, int64_t M, i
         return Q4_0_ERR_UNSUPPORTED;
     return Q4_0_OK;
 }
+}  // namespace q4_0
+
+namespace {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? Q4_0_OK : Q4_0_ERR_CUDA; }
 

@@ -7,7 +7,9 @@
 //   * x (bf16) is first rounded to binary16 into a scratch buffer, because a
 //     tcgen05 kind::f16 MMA takes A and B of one type and binary16 operand
 //     tiles keep the result well inside the error budget (bf16 weight tiles
-//     would not);
+//     would not); each row of x is scaled by a power of two first (its
+//     largest |x| into [2^14, 2^15)), which the epilogue undoes exactly, so
+//     any finite bf16 row fits binary16's range;
 //   * one CTA computes a 128 (weight rows) x TM (x rows) tile of y^T, TM a
 //     multiple of 16 chosen per call: the fewest tiles of at most 320 rows
 //     (every further tile dequantises each weight tile again; M = 272 is one
@@ -59,7 +61,7 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
 // Shared-memory and TMEM layout of a CTA for an x tile of `tm` rows.
 struct GemmLayout {
     uint32_t x_stage, d_cols, cols;
-    size_t bar_off, smem;
+    size_t bar_off, scale_off, smem;
     int num_bars;
     __host__ __device__ GemmLayout(int tm, int nx) {
         x_stage = (uint32_t)tm * 128;
@@ -67,7 +69,8 @@ struct GemmLayout {
         cols = pow2_at_least(d_cols + kNA * 32);
         bar_off = (size_t)nx * x_stage + (size_t)kNW * kWStageBytes;
         num_bars = 2 * kNW + 2 * nx + 2 * kNA + 2;
-        smem = 1024 + bar_off + num_bars * 8 + 16;
+        scale_off = bar_off + num_bars * 8 + 16;  // the tile's x-row scales (tm rounded up to 32 floats)
+        smem = 1024 + scale_off + (size_t)((tm + 31) / 32 * 32) * 4;
     }
 };
 
@@ -83,24 +86,74 @@ __device__ __forceinline__ void swap_mid_pairs(uint32_t &a, uint32_t &b) {
     b = hi;
 }
 
-// bf16 -> binary16 (round to nearest even), 8 elements per thread, in the k
-// order of the weight tiles (middle pair of every group of four swapped).
-__global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__ x,
-                                                       uint4 *__restrict__ x16, int64_t n8) {
+// Largest magnitude among the eight bf16 values of a 16-byte chunk, as bits
+// (for finite values the magnitude bits order like the magnitudes).
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 u) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) m = max(m, max(w[h] & 0x7FFFu, (w[h] >> 16) & 0x7FFFu));
+    return m;
+}
+
+// One row of x (bf16) -> binary16, scaled by 2^shift so that the row's
+// largest |x| lands in [2^14, 2^15): every element within 2^29 of it is then
+// a normal binary16 number and exact (bf16 has 8 significant bits), none
+// overflows, and tiny rows keep their precision.  xscale[m] = 2^-shift is
+// what the epilogue multiplies the fp32 accumulator by (exact: a power of
+// two).  Values are written in the k order of the weight tiles (middle pair
+// of every group of four swapped).  One CTA per row: the row's maximum, then
+// the conversion of the chunks the threads still hold in registers (rows
+// longer than 6144 reload the rest).  Small in registers, so that its CTAs
+// fit beside the running GEMM's and start as soon as it completes.
+constexpr int kXThreads = 256;
+constexpr int kXHeld = 3;  // chunks per thread kept in registers between the passes (K <= 6144)
+__global__ void __launch_bounds__(kXThreads, 8) x_to_f16_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x16,
+                                                              float *__restrict__ xscale, int kc8) {
     pdl_launch_dependents();
     pdl_wait();
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n8) return;
-    const uint4 u = __ldg(x + i);
-    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-    uint32_t out[4];
+    __shared__ uint32_t wmax[kXThreads / 32];
+    const int64_t base = (int64_t)blockIdx.x * kc8;
+    uint4 held[kXHeld];
+    uint32_t mb = 0;
 #pragma unroll
-    for (int h = 0; h < 4; ++h)
-        out[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16),
-                                       __uint_as_float(in[h] & 0xFFFF0000u)));
-    swap_mid_pairs(out[0], out[1]);
-    swap_mid_pairs(out[2], out[3]);
-    x16[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    for (int h = 0; h < kXHeld; ++h) {
+        const int i = threadIdx.x + h * kXThreads;
+        if (i < kc8) {
+            held[h] = __ldg(x + base + i);
+            mb = max(mb, bf16x8_absmax_bits(held[h]));
+        }
+    }
+    for (int i = threadIdx.x + kXHeld * kXThreads; i < kc8; i += kXThreads)
+        mb = max(mb, bf16x8_absmax_bits(__ldg(x + base + i)));
+    mb = __reduce_max_sync(0xffffffffu, mb);
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mb;
+    __syncthreads();
+    mb = 0;
+#pragma unroll
+    for (int w = 0; w < kXThreads / 32; ++w) mb = max(mb, wmax[w]);
+    int e = 0;
+    if (mb != 0) frexpf(__uint_as_float(mb << 16), &e);  // max |x| in [2^(e-1), 2^e)
+    const int shift = min(126, 15 - e);
+    const float up = ldexpf(1.0f, shift);
+    if (threadIdx.x == 0) xscale[blockIdx.x] = ldexpf(1.0f, -shift);
+    auto convert = [&](uint4 u) {
+        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            out[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16) * up,
+                                           __uint_as_float(in[h] & 0xFFFF0000u) * up));
+        swap_mid_pairs(out[0], out[1]);
+        swap_mid_pairs(out[2], out[3]);
+        return make_uint4(out[0], out[1], out[2], out[3]);
+    };
+#pragma unroll
+    for (int h = 0; h < kXHeld; ++h) {
+        const int i = threadIdx.x + h * kXThreads;
+        if (i < kc8) x16[base + i] = convert(held[h]);
+    }
+    for (int i = threadIdx.x + kXHeld * kXThreads; i < kc8; i += kXThreads) x16[base + i] = convert(__ldg(x + base + i));
 }
 
 // y = sum over splits of the partial tiles, in split order (deterministic);
@@ -170,8 +223,8 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
 template <bool kTall>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                float *__restrict__ y, float *__restrict__ part, int M, int N, int K, int TM, int ybf16,
-                unsigned int *err) {
+                float *__restrict__ y, float *__restrict__ part, const float *__restrict__ xscale, int M, int N,
+                int K, int TM, int ybf16, unsigned int *err) {
     constexpr int kNX = kTall ? kNXTall : kNXShort;
     const GemmLayout Cfg(TM, kNX);
     extern __shared__ uint8_t smem_raw[];
@@ -186,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *d_full = a_empty + kNA, *drain = d_full + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg.num_bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *xs_tile = reinterpret_cast<float *>(smem + Cfg.scale_off);  // [TM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * TM;
@@ -297,6 +351,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // weight row within the tile
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        // the tile's x-row scales: loaded now (in flight during the mainloop),
+        // put into shared memory for the epilogue after it -- loaded in the
+        // epilogue, each would wait behind the tensor-memory loads and the
+        // stores before it
+        float sv[(kMaxTileRows + 127) / 128];
+#pragma unroll
+        for (int t = 0; t < (kMaxTileRows + 127) / 128; ++t) {
+            const int i = threadIdx.x - 64 + 128 * t;
+            sv[t] = i < TM && m0 + i < M ? __ldg(xscale + m0 + i) : 0.f;
+        }
         bool ok = true;
         for (int ws = 0; ws < KWS && ok; ++ws) {
             const int wsl = ws % kNW;
@@ -342,7 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0) mbar_arrive(&w_empty[wsl]);
         }
-        // epilogue: D[row r][column m] -> y[m][n0 + r]
+        // epilogue: D[row r][column m] -> y[m][n0 + r], times the x row's
+        // scale 2^-shift (a power of two, so a K split's partial tiles sum
+        // to the same bits as the unsplit tile)
+#pragma unroll
+        for (int t = 0; t < (kMaxTileRows + 127) / 128; ++t) {
+            const int i = threadIdx.x - 64 + 128 * t;
+            if (i < (TM + 31) / 32 * 32) xs_tile[i] = sv[t];
+        }
+        named_bar_sync(1, 128);  // the four epilogue warps
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));
         if (ok) {
             tc_fence_after();
@@ -350,15 +422,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < TM; c += 32) {
                 uint32_t v[32];
                 tmem_ld32(d_tmem + lane_base + c, v);
+                // the 32 scales of these columns: eight 16-byte shared loads,
+                // outside the store predicates
+                float sc[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 t = reinterpret_cast<const float4 *>(xs_tile + c)[q];
+                    sc[4 * q] = t.x;
+                    sc[4 * q + 1] = t.y;
+                    sc[4 * q + 2] = t.z;
+                    sc[4 * q + 3] = t.w;
+                }
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int m = m0 + c + j;
+                    const float val = __uint_as_float(v[j]) * sc[j];
                     if (c + j < TM && m < M && n < N) {
                         if (out)
-                            out[(int64_t)m * N + n] = __uint_as_float(v[j]);
+                            out[(int64_t)m * N + n] = val;
                         else
-                            store_y(y, (int64_t)m * N + n, __uint_as_float(v[j]), ybf16 != 0);
+                            store_y(y, (int64_t)m * N + n, val, ybf16 != 0);
                     }
                 }
             }
@@ -398,8 +482,8 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, float *y, bool ybf16, float *part,
-                      int64_t M, int64_t N, int64_t K, cudaStream_t s, unsigned int *err) {
+cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, const uint8_t *wq, float *y,
+                      bool ybf16, float *part, int64_t M, int64_t N, int64_t K, cudaStream_t s, unsigned int *err) {
     const GemmLayout Cfg(TM, TM > 256 ? kNXTall : kNXShort);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -430,7 +514,7 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, fl
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM), (unsigned)splits);
-    e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr,
+    e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr, xscale,
                    (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
     if (e != cudaSuccess || splits == 1) return e;
     const int64_t n4 = M * N / 4;
@@ -443,6 +527,8 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const uint8_t *wq, fl
 namespace {
 
 int64_t x16_bytes(int64_t M, int64_t K) { return (M * K * 2 + 255) / 256 * 256; }
+// the per-row scales of x16 (fp32), after it
+int64_t xscale_bytes(int64_t M) { return (M * 4 + 255) / 256 * 256; }
 
 // Rows of x per CTA tile.  Each extra tile dequantises every weight tile
 // once more, but tiles of more than 256 rows run with a shallower x ring:
@@ -481,31 +567,31 @@ int gemm_splits(int64_t M, int64_t N, int64_t K, int sms) {
 }
 
 // The launch grids: M tiles in gridDim.y (at most 65535), N tiles in
-// gridDim.x, and the x pre-pass at one thread per eight elements.
+// gridDim.x, and the x pre-pass at one CTA per row of x.
 bool gemm_shape_supported(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 1) return false;
     const int tm = tile_rows(M);
-    return (M + tm - 1) / tm <= 65535 && (N + kTileN - 1) / kTileN <= 0x7FFFFFFF &&
-           (M * K / 8 + 255) / 256 <= 0x7FFFFFFF;
+    return (M + tm - 1) / tm <= 65535 && (N + kTileN - 1) / kTileN <= 0x7FFFFFFF && M <= 0x7FFFFFFF;
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {
-    size_t b = (size_t)x16_bytes(M, K);
+    size_t b = (size_t)x16_bytes(M, K) + (size_t)xscale_bytes(M);
     if (splits > 1) b += (size_t)splits * (size_t)M * (size_t)N * 4;
     return b;
 }
 
 cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, int splits, cudaStream_t s, unsigned int *err) {
-    void *x16 = workspace;
-    float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + x16_bytes(M, K));
-    const int64_t n8 = M * K / 8;
-    const int64_t blocks = (n8 + 255) / 256;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *x16 = ws;
+    float *xscale = reinterpret_cast<float *>(ws + x16_bytes(M, K));
+    float *part = reinterpret_cast<float *>(ws + x16_bytes(M, K) + xscale_bytes(M));
     if (!gemm_shape_supported(M, N, K)) return cudaErrorInvalidValue;
-    cudaError_t e = launch_pdl(x_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
-                               reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(x16), n8);
+    cudaError_t e = launch_pdl(x_to_f16_kernel, dim3((unsigned)M), dim3(kXThreads), 0, s,
+                               reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(x16), xscale,
+                               (int)(K / 8));
     if (e != cudaSuccess) return e;
-    return launch_tm(tile_rows(M), splits < 1 ? 1 : splits, x16, wq, y, ybf16, part, M, N, K, s, err);
+    return launch_tm(tile_rows(M), splits < 1 ? 1 : splits, x16, xscale, wq, y, ybf16, part, M, N, K, s, err);
 }
 
 }  // namespace q4_0

@@ -13,9 +13,9 @@
 //     4-slot shared-memory ring (no CTA-wide synchronisation in the loop);
 //   * lane (r, p) of a warp handles block pair p of row r of the item: nine
 //     conflict-free 32-bit shared loads, nibble unpack into fp16 pairs with
-//     the 0x6400 exponent trick, q - 8 exactly in fp16, and packed fp16
-//     FMAs against x (pre-scaled per block by a power of two so that the
-//     fp16 partial sums of one block cannot overflow);
+//     the 0x6400 exponent trick (q - 8 exactly), widened to fp32 and
+//     multiplied in fp32 with x held as binary16 (pre-scaled per block by a
+//     power of two so that the block's maximum sits just below 1);
 //   * scale apply per block in fp32: acc += partial * d * 2^e;
 //   * per item, a fixed butterfly over 16 lanes; per row, a fixed-order sum
 //     over chunks -- the result does not depend on timing.
@@ -57,7 +57,11 @@ __device__ __forceinline__ uint32_t h2u(half2 h) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// One Q4_0 block (scale bits + four code words) against MT rows of x.
+// One Q4_0 block (scale bits + four code words) against MT rows of x.  The
+// codes become exact binary16 integers (q - 8 for the low nibbles, 16 (q - 8)
+// for the high ones, which need no shift), are widened to fp32 and
+// multiplied by the binary16 x values in fp32; the high-nibble sums take the
+// exact factor 1/16 at the end.  Scale apply: one fp32 FMA per block.
 template <int MT>
 __device__ __forceinline__ void block_dot(uint32_t dbits, const uint32_t (&Q)[4],
                                           const uint4 *__restrict__ xq, int P,
@@ -66,32 +70,37 @@ __device__ __forceinline__ void block_dot(uint32_t dbits, const uint32_t (&Q)[4]
     const uint32_t kMagic = 0x64006400u;  // two fp16 1024.0
     const half2 k1032 = __floats2half2_rn(1032.0f, 1032.0f);
     const half2 k1152 = __floats2half2_rn(1152.0f, 1152.0f);
-    half2 v[16];
+    float2 v[16];
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
         const uint32_t q = Q[wi];
         const uint32_t q8 = q >> 8;
-        // lanes hold (element 4wi, 4wi+2), (16(4wi+16), 16(4wi+18)), (4wi+1, 4wi+3), (16(4wi+17), 16(4wi+19))
-        v[4 * wi + 0] = __hsub2(u2h((q & 0x000F000Fu) | kMagic), k1032);
-        v[4 * wi + 1] = __hsub2(u2h((q & 0x00F000F0u) | kMagic), k1152);
-        v[4 * wi + 2] = __hsub2(u2h((q8 & 0x000F000Fu) | kMagic), k1032);
-        v[4 * wi + 3] = __hsub2(u2h((q8 & 0x00F000F0u) | kMagic), k1152);
+        // pairs hold (element 4wi, 4wi+2), (16(4wi+16), 16(4wi+18)), (4wi+1, 4wi+3), (16(4wi+17), 16(4wi+19))
+        v[4 * wi + 0] = __half22float2(__hsub2(u2h((q & 0x000F000Fu) | kMagic), k1032));
+        v[4 * wi + 1] = __half22float2(__hsub2(u2h((q & 0x00F000F0u) | kMagic), k1152));
+        v[4 * wi + 2] = __half22float2(__hsub2(u2h((q8 & 0x000F000Fu) | kMagic), k1032));
+        v[4 * wi + 3] = __half22float2(__hsub2(u2h((q8 & 0x00F000F0u) | kMagic), k1152));
     }
     const float d = __half2float(__ushort_as_half((unsigned short)dbits));
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         const uint4 *xp = xq + (size_t)m * 8 * P;
-        half2 a0 = __floats2half2_rn(0.f, 0.f), a1 = a0;
+        float lo0 = 0.f, lo1 = 0.f, hi0 = 0.f, hi1 = 0.f;
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
             const uint4 X = xp[wi * P];
-            a0 = __hfma2(v[4 * wi + 0], u2h(X.x), a0);
-            a1 = __hfma2(v[4 * wi + 1], u2h(X.y), a1);
-            a0 = __hfma2(v[4 * wi + 2], u2h(X.z), a0);
-            a1 = __hfma2(v[4 * wi + 3], u2h(X.w), a1);
+            const float2 x0 = __half22float2(u2h(X.x)), x1 = __half22float2(u2h(X.y));
+            const float2 x2 = __half22float2(u2h(X.z)), x3 = __half22float2(u2h(X.w));
+            lo0 = fmaf(v[4 * wi + 0].x, x0.x, lo0);
+            lo1 = fmaf(v[4 * wi + 0].y, x0.y, lo1);
+            hi0 = fmaf(v[4 * wi + 1].x, x1.x, hi0);
+            hi1 = fmaf(v[4 * wi + 1].y, x1.y, hi1);
+            lo0 = fmaf(v[4 * wi + 2].x, x2.x, lo0);
+            lo1 = fmaf(v[4 * wi + 2].y, x2.y, lo1);
+            hi0 = fmaf(v[4 * wi + 3].x, x3.x, hi0);
+            hi1 = fmaf(v[4 * wi + 3].y, x3.y, hi1);
         }
-        const float2 f0 = __half22float2(a0), f1 = __half22float2(a1);
-        const float s = (f0.x + f0.y) + (f1.x + f1.y);
+        const float s = (lo0 + lo1) + 0.0625f * (hi0 + hi1);
         acc[m] = fmaf(s, d * sxb[(size_t)m * nb], acc[m]);
     }
 }
@@ -147,8 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
 
     // x -> shared memory, per (row m, block b): e = exponent of max|x| so
-    // that |x * 2^-e| < 1; quads of half2 in the order block_dot reads them;
-    // the high-nibble lanes carry an extra 1/16 (their codes arrive as 16q).
+    // that |x * 2^-e| < 1 (binary16: exact down to 2^-14 of the block's
+    // maximum, absolute error <= 2^(e-25) below); quads of half2 in the order
+    // block_dot reads them.
     for (int t = tid; t < MT * nb; t += kThreads) {
         const int m = t / nb, b = t - m * nb;
         float xv[32];
@@ -176,16 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             frexpf(amax, &e);
             e = max(-125, min(127, e));
         }
-        const float inv = ldexpf(1.0f, -e), inv16 = ldexpf(1.0f, -e - 4);
+        const float inv = ldexpf(1.0f, -e);
         sx[m * nb + b] = amax > 0.f ? ldexpf(1.0f, e) : 0.f;
         const int p = b >> 1, blk = b & 1;
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
             uint4 o;
             o.x = h2u(__floats2half2_rn(xv[4 * wi] * inv, xv[4 * wi + 2] * inv));
-            o.y = h2u(__floats2half2_rn(xv[4 * wi + 16] * inv16, xv[4 * wi + 18] * inv16));
+            o.y = h2u(__floats2half2_rn(xv[4 * wi + 16] * inv, xv[4 * wi + 18] * inv));
             o.z = h2u(__floats2half2_rn(xv[4 * wi + 1] * inv, xv[4 * wi + 3] * inv));
-            o.w = h2u(__floats2half2_rn(xv[4 * wi + 17] * inv16, xv[4 * wi + 19] * inv16));
+            o.w = h2u(__floats2half2_rn(xv[4 * wi + 17] * inv, xv[4 * wi + 19] * inv));
             xs[(size_t)(m * 8 + blk * 4 + wi) * P + p] = o;
         }
     }

@@ -12,7 +12,8 @@
 //     one MMA-warp iteration issues the slot's eight MMAs (the issuing warp
 //     shares its scheduler with the dequant warps, so fewer, larger
 //     iterations keep it off the critical path);
-//   * B = x: a small kernel first rounds x to binary16 once per call, already
+//   * B = x: a small kernel first rounds x to binary16 once per call (each
+//     row scaled by a power of two that the stores of y undo exactly), already
 //     in the 128-byte-swizzled K-major tiles the MMA reads (rows >= M zero),
 //     into a workspace of TM * K * 2 bytes; every CTA then brings in each
 //     stage's x tile with one bulk copy.  Converting inside every CTA would
@@ -67,8 +68,9 @@ struct Cfg {
     static constexpr uint32_t kCols = cols_pow2(kDCols + kNA * (kKB / 2));
     static constexpr size_t kOffW = (size_t)kNX * kXStage;
     static constexpr size_t kOffBars = kOffW + (size_t)kNW * kWStageBytes;
-    static constexpr int kNumBars = 2 * kNW + 2 * kNX + 2 * kNA + 2;
-    static constexpr size_t kSmem = 1024 + kOffBars + kNumBars * 8 + 16;
+    static constexpr int kNumBars = 2 * kNW + 2 * kNX + 2 * kNA + 3;
+    static constexpr size_t kOffScale = kOffBars + ((kNumBars * 8 + 16 + 15) / 16) * 16;  // TM floats
+    static constexpr size_t kSmem = 1024 + kOffScale + TM * 4;
 };
 
 __device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
@@ -120,45 +122,101 @@ __device__ __forceinline__ void swap_mid_pairs(uint32_t &a, uint32_t &b) {
     b = hi;
 }
 
+// Largest magnitude among the eight bf16 values of a 16-byte chunk, as bits
+// (for finite values the magnitude bits order like the magnitudes).
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 u) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) m = max(m, max(w[h] & 0x7FFFu, (w[h] >> 16) & 0x7FFFu));
+    return m;
+}
+
 // x (bf16, [M][K]) -> the binary16 B tiles of gemv_tc_kernel, and zeroed
-// split-K tile counters for it: stage u (256 k)
-// is four atoms [TM rows x 64 k]; in an atom, row m is 128 bytes whose
-// 16-byte chunk c sits at position c ^ (m & 7) (the 128-byte swizzle named in
-// the MMA's shared-memory descriptor), values in the k order of the weight
-// tiles; rows m >= M are zero.  One thread per 16-byte chunk.
+// split-K tile counters for it.  Each row is scaled by 2^shift so that its
+// largest |x| lands in [2^14, 2^15) -- every element within 2^29 of it is a
+// normal binary16 number and exact, none overflows, and tiny rows keep their
+// precision -- and xscale[m] = 2^-shift (a power of two) is what the
+// kernel's stores multiply by.  Stage u (256 k) is four atoms [TM rows x
+// 64 k]; in an atom, row m is 128 bytes whose 16-byte chunk c sits at
+// position c ^ (m & 7) (the 128-byte swizzle named in the MMA's shared-memory
+// descriptor), values in the k order of the weight tiles; rows m >= M are
+// zero.  One CTA per row of the tile: the row's maximum, then the
+// conversion of the chunks the threads still hold in registers (rows longer
+// than 8192 reload the rest).  128 threads of at most 56 registers, so that
+// its CTAs fit beside two CTAs of the running decode kernel and start as
+// soon as it completes.
+constexpr int kXThreads = 128;
+constexpr int kXHeld = 8;  // chunks per thread kept in registers between the passes (K <= 8192)
 template <int TM>
-__global__ void __launch_bounds__(256) x_tiles_kernel(const uint16_t *__restrict__ x, uint4 *__restrict__ xt,
-                                                      int M, int K, unsigned int *__restrict__ tile_cnt,
-                                                      int ncnt) {
+__global__ void __launch_bounds__(kXThreads, 9) x_tiles_kernel(const uint16_t *__restrict__ x, uint4 *__restrict__ xt,
+                                                            float *__restrict__ xscale, int M, int K,
+                                                            unsigned int *__restrict__ tile_cnt, int ncnt) {
     pdl_launch_dependents();
     pdl_wait();  // x may come from the previous kernel (and the last one has read its counters)
     if (blockIdx.x == 0)  // the split-K tile counters of the matmul kernel that follows
-        for (int i = threadIdx.x; i < ncnt; i += blockDim.x) tile_cnt[i] = 0u;
+        for (int i = threadIdx.x; i < ncnt; i += kXThreads) tile_cnt[i] = 0u;
+    __shared__ uint32_t wmax[kXThreads / 32];
+    const int m = blockIdx.x;
     const int kc8 = K / 8;
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)TM * kc8) return;
-    const int m = (int)(i / kc8), kc = (int)(i - (int64_t)m * kc8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (m < M) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)m * K) + kc);
-        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-        uint32_t o[4];
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)m * K);
+    uint4 held[kXHeld];
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
-            o[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16), __uint_as_float(in[h] & 0xFFFF0000u)));
-        swap_mid_pairs(o[0], o[1]);
-        swap_mid_pairs(o[2], o[3]);
-        v = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int h = 0; h < kXHeld; ++h) held[h] = make_uint4(0, 0, 0, 0);
+    uint32_t mb = 0;
+    if (m < M) {
+#pragma unroll
+        for (int h = 0; h < kXHeld; ++h) {
+            const int kc = threadIdx.x + h * kXThreads;
+            if (kc < kc8) {
+                held[h] = __ldg(src + kc);
+                mb = max(mb, bf16x8_absmax_bits(held[h]));
+            }
+        }
+        for (int kc = threadIdx.x + kXHeld * kXThreads; kc < kc8; kc += kXThreads)
+            mb = max(mb, bf16x8_absmax_bits(__ldg(src + kc)));
     }
-    const int u = kc >> 5, a = (kc >> 3) & 3, c = kc & 7;
-    xt[((int64_t)(u * 4 + a) * TM + m) * 8 + (c ^ (m & 7))] = v;
+    mb = __reduce_max_sync(0xffffffffu, mb);
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mb;
+    __syncthreads();
+    mb = 0;
+#pragma unroll
+    for (int w = 0; w < kXThreads / 32; ++w) mb = max(mb, wmax[w]);
+    int e = 0;
+    if (mb != 0) frexpf(__uint_as_float(mb << 16), &e);  // max |x| in [2^(e-1), 2^e)
+    const int shift = min(126, 15 - e);
+    const float up = ldexpf(1.0f, shift);
+    if (threadIdx.x == 0 && m < M) xscale[m] = ldexpf(1.0f, -shift);
+    auto store = [&](int kc, uint4 u, bool live) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (live) {
+            const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                o[h] = h2u(__floats2half2_rn(__uint_as_float(in[h] << 16) * up,
+                                             __uint_as_float(in[h] & 0xFFFF0000u) * up));
+            swap_mid_pairs(o[0], o[1]);
+            swap_mid_pairs(o[2], o[3]);
+            v = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        const int u4 = kc >> 5, a = (kc >> 3) & 3, c = kc & 7;
+        xt[((int64_t)(u4 * 4 + a) * TM + m) * 8 + (c ^ (m & 7))] = v;
+    };
+#pragma unroll
+    for (int h = 0; h < kXHeld; ++h) {
+        const int kc = threadIdx.x + h * kXThreads;
+        if (kc < kc8) store(kc, held[h], m < M);
+    }
+    for (int kc = threadIdx.x + kXHeld * kXThreads; kc < kc8; kc += kXThreads)
+        store(kc, m < M ? __ldg(src + kc) : make_uint4(0, 0, 0, 0), m < M);
 }
 
 template <int TM>
 __global__ void __launch_bounds__(kThreads, 2)
     gemv_tc_kernel(const uint4 *__restrict__ xt, const __grid_constant__ CUtensorMap wmap,
                    float *__restrict__ y, float *__restrict__ part, unsigned int *__restrict__ tile_cnt,
-                   int M, int N, int K, int ybf16, unsigned int *err) {
+                   const float *__restrict__ xscale, int M, int N, int K, int ybf16, unsigned int *err) {
     using C = Cfg<TM>;
     constexpr int kNX = C::kNX;
     extern __shared__ uint8_t smem_raw[];
@@ -170,9 +228,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *w_full = bars, *w_empty = bars + kNW;
     uint64_t *x_full = bars + 2 * kNW, *x_empty = x_full + kNX;
     uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNA;
-    uint64_t *d_full = a_empty + kNA, *drain = d_full + 1;
+    uint64_t *d_full = a_empty + kNA, *drain = d_full + 1, *s_full = drain + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *xs_smem = reinterpret_cast<float *>(smem + C::kOffScale);  // the x rows' scales [TM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = gridDim.x;                 // CTAs per tile, along K
@@ -197,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mbar_init(d_full, 1);
         mbar_init(drain, 1);
+        mbar_init(s_full, 1);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&wmap);
@@ -237,6 +297,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             bool ok = true;
             for (int ws = 0; ok && ws < kNW && ws < nW; ++ws) ok = issue_w(ws);
             pdl_wait();  // the x tiles come from the previous kernel
+            // the x rows' scales for the stores of y (the workspace holds room
+            // for 64 of them, so the copy stays inside it for any M)
+            mbar_arrive_expect_tx(s_full, TM * 4);
+            bulk_g2s(xs_smem, xscale, TM * 4, s_full);
             for (int ws = 0; ok && ws < nW; ++ws) {
                 ok = issue_x(ws);
                 if (ok && ws + kNW < nW) ok = issue_w(ws + kNW);
@@ -246,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (i >= 0) mbar_drain(&w_full[i % kNW], (i / kNW) & 1);
             for (int i = issued_x - kNX; i < issued_x; ++i)
                 if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
+            mbar_drain(s_full, 0);
         }
         __syncwarp();  // lanes 1..31 wait for the producer lane before the closing barriers
     } else if (warp == 1) {
@@ -358,6 +423,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         // epilogue (warps 2..5 cover the four lane quarters): D -> partial tile
         if (half == 0) {
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));
+            // one K split stores y and needs the x rows' scales
+            if (ok && S == 1) ok = __all_sync(0xffffffffu, mbar_wait(s_full, 0, abort_flag, err));
             if (ok) {
                 tc_fence_after();
                 uint32_t v[16];
@@ -370,11 +437,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tmem_ld16(d_tmem + lane_base + c, v);
                     tmem_wait_ld();
 #pragma unroll
+                    float sc[16];  // outside the store predicates: four 16-byte shared loads
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 t = reinterpret_cast<const float4 *>(xs_smem + c)[q];
+                        sc[4 * q] = t.x;
+                        sc[4 * q + 1] = t.y;
+                        sc[4 * q + 2] = t.z;
+                        sc[4 * q + 3] = t.w;
+                    }
+#pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = c + j;
                         if (m >= M) break;
                         if (S == 1) {
-                            if (n < N) store_y(y, (int64_t)m * N + n, __uint_as_float(v[j]), ybf16 != 0);
+                            if (n < N) store_y(y, (int64_t)m * N + n, __uint_as_float(v[j]) * sc[j], ybf16 != 0);
                         } else {
                             pt[(size_t)m * kTileN] = __uint_as_float(v[j]);
                         }
@@ -432,7 +509,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int g = g0 + h * kThreads;
                     if (g >= groups) continue;
                     const int m = g / kGroupsPerRow, n = n0 + 4 * (g - m * kGroupsPerRow);
-                    const float s4[4] = {sum[h].x, sum[h].y, sum[h].z, sum[h].w};
+                    const float sc = __ldg(xscale + m);  // the x row's 2^-shift (exact)
+                    const float s4[4] = {sum[h].x * sc, sum[h].y * sc, sum[h].z * sc, sum[h].w * sc};
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         if (n + j < N) store_y(y, (int64_t)m * N + n + j, s4[j], ybf16 != 0);
@@ -470,13 +548,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Workspace: the x tiles, then room for 2 * SMs partial tiles (S * tiles
-// never exceeds that when S > 1), then 2 * SMs tile counters.
+// Workspace: the x tiles, the x rows' scales, then room for 2 * SMs partial
+// tiles (S * tiles never exceeds that when S > 1), then 2 * SMs tile
+// counters.
 struct WorkspaceLayout {
-    size_t part_off, cnt_off, bytes;
+    size_t scale_off, part_off, cnt_off, bytes;
     WorkspaceLayout(int tm, int64_t K, int sms) {
         const size_t xt = (size_t)tm * (size_t)K * 2;
-        part_off = (xt + 255) / 256 * 256;
+        scale_off = (xt + 255) / 256 * 256;
+        part_off = scale_off + 256;  // tm <= 32 floats
         const size_t pb = (size_t)2 * (size_t)sms * kTileN * (size_t)tm * 4;
         cnt_off = part_off + pb;
         bytes = cnt_off + ((size_t)2 * (size_t)sms * 4 + 255) / 256 * 256 * (sms > 0 ? 1 : 0);
@@ -518,14 +598,14 @@ cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const WorkspaceLayout L(TM, K, sms);
     float *part = reinterpret_cast<float *>(ws + L.part_off);
+    float *xscale = reinterpret_cast<float *>(ws + L.scale_off);
     unsigned int *cnt = reinterpret_cast<unsigned int *>(ws + L.cnt_off);
-    const int64_t chunks = (int64_t)TM * (K / 8);
-    e = launch_pdl(x_tiles_kernel<TM>, dim3((unsigned)((chunks + 255) / 256)), dim3(256), 0, s, x,
-                   reinterpret_cast<uint4 *>(ws), (int)M, (int)K, cnt, S > 1 ? (int)tiles : 0);
+    e = launch_pdl(x_tiles_kernel<TM>, dim3((unsigned)TM), dim3(kXThreads), 0, s, x, reinterpret_cast<uint4 *>(ws),
+                   xscale, (int)M, (int)K, cnt, S > 1 ? (int)tiles : 0);
     if (e != cudaSuccess) return e;
     return launch_pdl(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads), C::kSmem, s,
-                      reinterpret_cast<const uint4 *>(ws), wmap, y, part, cnt, (int)M, (int)N, (int)K,
-                      ybf16 ? 1 : 0, err);
+                      reinterpret_cast<const uint4 *>(ws), wmap, y, part, cnt, static_cast<const float *>(xscale),
+                      (int)M, (int)N, (int)K, ybf16 ? 1 : 0, err);
 }
 
 }  // namespace

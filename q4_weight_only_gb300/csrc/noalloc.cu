@@ -54,19 +54,14 @@ void *scratch_for_current_device() {
     return g_scratch_ptr[dev];
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" int q4_0_gemm_noalloc(const uint16_t *x, const uint8_t *wq, float *y, int64_t M,
                                  int64_t N, int64_t K, void *stream) {
-    if (!x || !wq || !y) return Q4_0_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return Q4_0_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(wq) || !aligned16(y)) return Q4_0_ERR_INVALID_ARG;
-    if (K % 256 != 0) return Q4_0_ERR_UNSUPPORTED;
-    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 24) || N * K > (1ll << 40) ||
-        M * N > (1ll << 40))
-        return Q4_0_ERR_UNSUPPORTED;
+    // the same checks, in the same order, as q4_0_gemm
+    const int st = q4_0::check_matmul_args(x, wq, y, M, N, K);
+    if (st != Q4_0_OK) return st;
+    if (!q4_0::gemm_shape_supported(M, N, K)) return Q4_0_ERR_UNSUPPORTED;
     if (M * K > (int64_t)(Q4_0_NOALLOC_SCRATCH_BYTES / 2) ||
         q4_0::gemm_workspace_bytes(M, N, K, 1) > Q4_0_NOALLOC_SCRATCH_BYTES)
         return Q4_0_ERR_WORKSPACE;
@@ -74,6 +69,7 @@ extern "C" int q4_0_gemm_noalloc(const uint16_t *x, const uint8_t *wq, float *y,
     if (!scratch) return Q4_0_ERR_CUDA;
     unsigned int *err = q4_0::device_error_word();
     if (!err) return Q4_0_ERR_CUDA;
+    // K is never split here: the array holds the binary16 copy of x only
     const cudaError_t e =
         q4_0::launch_gemm(x, wq, y, false, M, N, K, scratch, 1, static_cast<cudaStream_t>(stream), err);
     return e == cudaSuccess ? Q4_0_OK : Q4_0_ERR_CUDA;

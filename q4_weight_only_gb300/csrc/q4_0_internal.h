@@ -35,6 +35,12 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 // Device error word of the current device (a __device__ variable's address).
 unsigned int *device_error_word();
 
+// Validation shared by every matmul entry point: a Q4_0 status code.
+// `any_k`: K % 32 == 0 is enough (the dispatcher pads other K to a multiple
+// of 256); the kernel-alone entry points need K % 256 == 0.
+int check_matmul_args(const void *x, const void *wq, const void *y, int64_t M, int64_t N, int64_t K,
+                      bool any_k = false);
+
 cudaError_t launch_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, cudaStream_t s,
                             unsigned int *err);
 

@@ -53,31 +53,35 @@ def test_weight_bytes(lib):
 
 
 def test_workspace_sizes(lib):
+    a256 = lambda b: (b + 255) // 256 * 256
+    # batched decode (no device here, so no room for split-K partials): x as
+    # binary16 tiles of 16 or 32 rows, then 256 bytes for the rows' scales
+    tc = lambda tm, K: a256(tm * K * 2) + 256
+    # GEMM (unsplit): x as binary16, then the rows' scales
+    gemm = lambda M, K: a256(M * K * 2) + a256(M * 4)
     assert lib.q4_0_matmul_workspace_bytes(1, 5120, 5120) == 0
     assert lib.q4_0_matmul_workspace_bytes(2, 5120, 5120) == 0
-    # batched decode: x as binary16 tiles of 16 or 32 rows
-    assert lib.q4_0_matmul_workspace_bytes(3, 5120, 5120) == 16 * 5120 * 2
-    assert lib.q4_0_matmul_workspace_bytes(16, 5120, 17408) == 16 * 17408 * 2
-    assert lib.q4_0_matmul_workspace_bytes(17, 5120, 5120) == 32 * 5120 * 2
-    assert lib.q4_0_matmul_workspace_bytes(32, 5120, 5120) == 32 * 5120 * 2
+    assert lib.q4_0_matmul_workspace_bytes(3, 5120, 5120) == tc(16, 5120)
+    assert lib.q4_0_matmul_workspace_bytes(16, 5120, 17408) == tc(16, 17408)
+    assert lib.q4_0_matmul_workspace_bytes(17, 5120, 5120) == tc(32, 5120)
+    assert lib.q4_0_matmul_workspace_bytes(32, 5120, 5120) == tc(32, 5120)
     for M in (1, 2, 3, 16, 17, 32):
         assert lib.q4_0_gemv_workspace_bytes(M, 5120) == lib.q4_0_matmul_workspace_bytes(M, 7, 5120)
     assert lib.q4_0_gemv_workspace_bytes(33, 5120) == 0
     # K % 256 != 0: zero-padded copies of W and x (256-byte aligned), then the
     # padded problem's own scratch
-    a256 = lambda b: (b + 255) // 256 * 256
     assert lib.q4_0_matmul_workspace_bytes(1, 300, 96) == a256(300 * 8 * 18) + a256(1 * 256 * 2)
     assert lib.q4_0_matmul_workspace_bytes(16, 300, 5152) == (a256(300 * 168 * 18) + a256(16 * 5376 * 2)
-                                                               + 16 * 5376 * 2)
-    assert lib.q4_0_matmul_workspace_bytes(64, 300, 288) >= a256(300 * 16 * 18) + a256(64 * 512 * 2) + 64 * 512 * 2
-    assert lib.q4_0_matmul_workspace_bytes(33, 5120, 5120) == 33 * 5120 * 2
+                                                               + tc(16, 5376))
+    assert lib.q4_0_matmul_workspace_bytes(64, 300, 288) >= a256(300 * 16 * 18) + a256(64 * 512 * 2) + gemm(64, 512)
+    assert lib.q4_0_matmul_workspace_bytes(33, 5120, 5120) == gemm(33, 5120)
     assert lib.q4_0_gemm_workspace_bytes(3, 128, 256) % 256 == 0
     # one or two rows with K past 65536 (x no longer fits shared memory) take
     # the tensor-core decode and its x tiles
     for M in (1, 2):
         assert lib.q4_0_matmul_workspace_bytes(M, 300, 65536) == 0
-        assert lib.q4_0_matmul_workspace_bytes(M, 300, 65792) == 16 * 65792 * 2
-        assert lib.q4_0_gemv_workspace_bytes(M, 131072) == 16 * 131072 * 2
+        assert lib.q4_0_matmul_workspace_bytes(M, 300, 65792) == tc(16, 65792)
+        assert lib.q4_0_gemv_workspace_bytes(M, 131072) == tc(16, 131072)
 
 
 def test_invalid_arguments_rejected_before_cuda(lib):

@@ -59,15 +59,16 @@ def test_dispatch_matches_kernels_bitwise():
 
 
 def test_gemm_split_k_matches_unsplit():
-    """A workspace with room only for x runs the GEMM unsplit; the default
-    workspace may split K (few output tiles). Both meet the tolerance."""
+    """A workspace with room only for x (binary16, and the rows' scales) runs
+    the GEMM unsplit; the default workspace may split K (few output tiles).
+    Both meet the tolerance."""
     q4 = lib()
     M, N, K = 272, 384, 5120                       # 3 x 2 output tiles: K gets split
     x, wq = case(8100, M, N, K)
     xd, wd = x_dev(x), wq_dev(wq)
     split = q4.gemm(xd, wd, N, K)
     ws_x_only = torch.empty(q4.lib().q4_0_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
-    small = ws_x_only[: (M * K * 2 + 255) // 256 * 256]
+    small = ws_x_only[: (M * K * 2 + 255) // 256 * 256 + (M * 4 + 255) // 256 * 256]
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     st = q4.lib().q4_0_gemm(xd.data_ptr(), wd.data_ptr(), y.data_ptr(), M, N, K, small.data_ptr(),
                             small.numel(), None)
@@ -372,9 +373,10 @@ def test_matmul_host_equals_device_call():
 def test_graph_capture_replays_bitwise():
     """A decode step captured into a CUDA graph (decode, batched decode and
     GEMM calls back to back under programmatic dependent launch, each with
-    its own workspace) replays to the same bits as the direct calls."""
+    its own workspace) replays to the same bits as the direct calls, and
+    every replayed output meets the oracle tolerance."""
     q4 = lib()
-    calls = []
+    calls, host = [], []
     for M, N, K in ((1, 1000, 5120), (2, 300, 1024), (16, 520, 2048), (40, 300, 1024), (272, 260, 1024),
                     (1, 100, 96)):
         x, wq = case(8600 + M + N, M, N, K)
@@ -382,6 +384,7 @@ def test_graph_capture_replays_bitwise():
         ws = torch.empty(max(1, q4.lib().q4_0_matmul_workspace_bytes(M, N, K)), dtype=torch.uint8, device="cuda")
         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
         calls.append((xd, wd, N, K, ws, y))
+        host.append((x, wq, N, K))
     st = torch.cuda.Stream()
     with torch.cuda.stream(st):
         ref = [q4.matmul(xd, wd, N, K, workspace=ws, stream=st).clone() for xd, wd, N, K, ws, _ in calls]
@@ -397,6 +400,8 @@ def test_graph_capture_replays_bitwise():
             st.synchronize()
             for r, (*_, y) in zip(ref, calls):
                 assert torch.equal(y, r)
+    for (x, wq, N, K), (*_, y) in zip(host, calls):
+        check_full(y, x, wq, N, K)
     assert q4.device_error() == 0
 
 
@@ -421,4 +426,17 @@ def test_concurrent_streams():
     torch.cuda.synchronize()
     for y, ref in outs:
         assert torch.equal(y, ref)
+    assert q4.device_error() == 0
+
+
+def test_prefill_down_m512_every_output():
+    """The down projection (K = 17408: 68 weight stages per tile, the longest
+    k loop of the configurations) at M = 512, every output against the
+    oracle rather than a sample."""
+    q4 = lib()
+    N, K = synth.SHAPES["down"]
+    wq = oracle.get().quantize(synth.prefill_weights("down"))
+    x = synth.prefill_x("down", 512)
+    y = q4.matmul(x_dev(x), wq_dev(wq), N, K)
+    check_full(y, x, wq, N, K)
     assert q4.device_error() == 0

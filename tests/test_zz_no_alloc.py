@@ -4,7 +4,8 @@ q4_0_gemm_noalloc serves callers that cannot allocate device memory: its
 scratch is a fixed array inside the library.  Called straight through the C
 ABI, twice in a row on different inputs, it must give what the workspace
 entry point gives, within the tolerance the other tests use, and it must
-refuse sizes its array cannot hold.  This file is collected last on purpose.
+refuse sizes its array cannot hold; sampled rows are also checked against the
+oracle.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -35,9 +36,13 @@ def test_noalloc_matches_gemm_on_two_calls():
         assert _call_noalloc(q4, xd, wd, y, M, N, K) == q4.OK
         torch.cuda.synchronize()
         rows = np.arange(0, M, max(1, M // 64))
-        _, absum = o.matmul(x[rows], wq, N, K)
+        y_ref, absum = o.matmul(x[rows], wq, N, K)
         got = y[torch.from_numpy(rows).cuda()].double().cpu().numpy()
         exp = ref[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+        # against the oracle, and against the workspace entry point (which
+        # may split K and so sum in another order: tolerance, not bits)
+        r = oracle.check(got, y_ref, absum)
+        assert r["ok"], r
         r = oracle.check(got, exp, absum)
         assert r["ok"], r
     assert q4.device_error() == 0
