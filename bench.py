@@ -497,13 +497,18 @@ def workload_name(w, M, layers, grouped=False):
                        f"four matrices per step, {layers} layer copies"}[w]
 
 
+# q4_0_matmul sends M up to this to the decode kernels, larger M to the GEMM
+DECODE_MAX_M = 64
+
+
 def kernels_per_call(q4, M, N, K):
     """Kernels one q4_0_matmul call launches: the integer-dot decode
-    (M <= 2); x tiles + tensor-core decode (3 <= M <= 32); x -> binary16 +
-    GEMM, plus the split-K sum when the workspace holds partial tiles."""
+    (M <= 2); x tiles + tensor-core decode (3 <= M <= DECODE_MAX_M); x ->
+    binary16 + GEMM, plus the split-K sum when the workspace holds partial
+    tiles."""
     if M <= 2:
         return 1
-    if M <= 32:
+    if M <= DECODE_MAX_M:
         return 2
     x16 = (M * K * 2 + 255) // 256 * 256 + (M * 4 + 255) // 256 * 256  # x as binary16 and its row scales
     return 3 if q4.lib().q4_0_gemm_workspace_bytes(M, N, K) > x16 else 2
@@ -514,8 +519,8 @@ def dominant_kernel(M, grouped=False):
         return f"gemv_dp4a_grouped_kernel<{M}>"
     if M <= 2:
         return f"gemv_dp4a_kernel<{M}>"
-    if M <= 32:
-        return f"gemv_tc_kernel<{16 if M <= 16 else 32}>"
+    if M <= DECODE_MAX_M:
+        return f"gemv_tc_kernel<{16 if M <= 16 else (32 if M <= 32 else 64)}>"
     return "gemm_kernel"
 
 

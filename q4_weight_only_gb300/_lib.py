@@ -283,7 +283,7 @@ def matmul_alloc(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.T
 
 def gemv(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
          workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
-    """The decode kernels alone (M <= 32), through q4_0_gemv_ws."""
+    """The decode kernels alone (M <= 64), through q4_0_gemv_ws."""
     M, out = _mm_args(x, wq, N, K, out)
     ws, wsb = _workspace(int(lib().q4_0_gemv_workspace_bytes(M, K)), x.device, workspace)
     _check(lib().q4_0_gemv_ws(x.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,

@@ -175,7 +175,7 @@ size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 }
 
 size_t q4_0_gemv_workspace_bytes(int64_t M, int64_t K) {
-    if (M < 1 || M > 32 || K < 1) return 0;
+    if (M < 1 || M > kGemvMaxM || K < 1) return 0;
     return gemv_workspace_bytes(M, K);
 }
 
@@ -184,7 +184,7 @@ size_t q4_0_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     // other K: the zero-padded copies of W and x, then the padded problem's own
     const size_t pad = pad_bytes(M, N, K);
     const int64_t kp = padded_k(K);
-    if (M <= 32) return pad + q4_0_gemv_workspace_bytes(M, kp);
+    if (M <= kDecodeMaxM) return pad + q4_0_gemv_workspace_bytes(M, kp);
     return pad + q4_0_gemm_workspace_bytes(M, N, kp);
 }
 
@@ -195,7 +195,7 @@ int gemv_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int
                  void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
-    if (M > 32 || !gemv_shape_supported(M, N, K)) return Q4_0_ERR_UNSUPPORTED;
+    if (M > kGemvMaxM || !gemv_shape_supported(M, N, K)) return Q4_0_ERR_UNSUPPORTED;
     const size_t need = gemv_workspace_bytes(M, K);
     if (need && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return Q4_0_ERR_WORKSPACE;
@@ -227,7 +227,8 @@ int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, i
     int st = check_matmul_args(x, wq, y, M, N, K, true);
     if (st != Q4_0_OK) return st;
     const int64_t kk = K % 256 != 0 ? padded_k(K) : K;
-    if (M <= 32 ? !gemv_shape_supported(M, N, kk) : !gemm_shape_supported(M, N, kk)) return Q4_0_ERR_UNSUPPORTED;
+    if (M <= kDecodeMaxM ? !gemv_shape_supported(M, N, kk) : !gemm_shape_supported(M, N, kk))
+        return Q4_0_ERR_UNSUPPORTED;
     if (K % 256 != 0) {
         // copy W and x, zero-padded to a multiple of 256, then run the padded problem
         const size_t pad = pad_bytes(M, N, K);
@@ -241,10 +242,11 @@ int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, i
         void *rest = static_cast<uint8_t *>(workspace) + pad;
         const size_t rest_bytes = workspace_bytes - pad;
         const int64_t kp = padded_k(K);
-        if (M <= 32) return gemv_ws_impl(xp, wqp, y, ybf16, M, N, kp, rest_bytes ? rest : nullptr, rest_bytes, stream);
+        if (M <= kDecodeMaxM)
+            return gemv_ws_impl(xp, wqp, y, ybf16, M, N, kp, rest_bytes ? rest : nullptr, rest_bytes, stream);
         return gemm_impl(xp, wqp, y, ybf16, M, N, kp, rest, rest_bytes, stream);
     }
-    if (M <= 32) return gemv_ws_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
+    if (M <= kDecodeMaxM) return gemv_ws_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
     return gemm_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
 }
 
@@ -274,7 +276,7 @@ int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y, int64_t M, int64_t
               void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
-    if (M > 32) return Q4_0_ERR_UNSUPPORTED;
+    if (M > kGemvMaxM) return Q4_0_ERR_UNSUPPORTED;
     return matmul_alloc_impl(x, wq, y, false, M, N, K, stream);
 }
 
@@ -314,7 +316,7 @@ int q4_0_matmul_grouped(int G, const uint16_t *const *x, const uint8_t *const *w
         const int st = check_matmul_args(x[g], wq[g], y[g], M, N[g], K[g], true);
         if (st != Q4_0_OK) return st;
         const int64_t kk = K[g] % 256 != 0 ? padded_k(K[g]) : K[g];
-        if (M <= 32 ? !gemv_shape_supported(M, N[g], kk) : !gemm_shape_supported(M, N[g], kk))
+        if (M <= kDecodeMaxM ? !gemv_shape_supported(M, N[g], kk) : !gemm_shape_supported(M, N[g], kk))
             return Q4_0_ERR_UNSUPPORTED;
     }
     unsigned int *err = device_error_word();

@@ -49,6 +49,10 @@ constexpr int kNW = 3, kNA = 4;              // weight and A-slot ring depths
 // 32 KB there, and L2 latency under the stream needs the depth); a tall tile
 // (up to kMaxTileRows rows, 40 KB a stage) fits four
 constexpr int kNXShort = 5, kNXTall = 4;
+// Tiles of 96..128 rows keep two CTAs on an SM (twice the dequantising warps,
+// which bind the GEMM at small M) only with a three-stage x ring; up to 80
+// rows five stages fit beside a second CTA.
+constexpr int kNXPair = 3, kPairMaxRows = 128;
 constexpr int kMaxTileRows = 320;
 constexpr int kThreads = 192;
 
@@ -73,6 +77,16 @@ struct GemmLayout {
         smem = 1024 + scale_off + (size_t)((tm + 31) / 32 * 32) * 4;
     }
 };
+
+// x ring depth for a tile of tm rows when the launch has `ctas` CTAs on
+// `sms` SMs: the shallow ring where it lets a second CTA share the SM
+// (shared memory and tensor memory both fit two) and there are more CTAs
+// than SMs to pair up; a CTA alone on its SM keeps the deep ring.
+int x_ring_stages(int tm, int64_t ctas, int sms) {
+    if (tm > 256) return kNXTall;
+    if (tm > 80 && tm <= kPairMaxRows && ctas > sms) return kNXPair;
+    return kNXShort;
+}
 
 __device__ __forceinline__ half2 u2h(uint32_t u) { return *reinterpret_cast<half2 *>(&u); }
 __device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -220,12 +234,12 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
 
 // kTall: x tiles of more than 256 rows (two TMA boxes per x stage, a second
 // MMA per k step); a separate instantiation keeps the common path unchanged.
-template <bool kTall>
+// kNX: stages of the x ring.
+template <bool kTall, int kNX>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 float *__restrict__ y, float *__restrict__ part, const float *__restrict__ xscale, int M, int N,
                 int K, int TM, int ybf16, unsigned int *err) {
-    constexpr int kNX = kTall ? kNXTall : kNXShort;
     const GemmLayout Cfg(TM, kNX);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -484,7 +498,12 @@ EncodeTiledFn encode_fn() {
 
 cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, const uint8_t *wq, float *y,
                       bool ybf16, float *part, int64_t M, int64_t N, int64_t K, cudaStream_t s, unsigned int *err) {
-    const GemmLayout Cfg(TM, TM > 256 ? kNXTall : kNXShort);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = ((N + kTileN - 1) / kTileN) * ((M + TM - 1) / TM) * splits;
+    const int nx = x_ring_stages(TM, ctas, device_sm_count(dev));
+    const GemmLayout Cfg(TM, nx);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap xmap, wmap;
@@ -510,8 +529,9 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
             return cudaErrorInvalidValue;
     }
     const bool tall = TM > 256;
-    auto kernel = tall ? gemm_kernel<true> : gemm_kernel<false>;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
+    auto kernel = tall ? gemm_kernel<true, kNXTall>
+                       : (nx == kNXPair ? gemm_kernel<false, kNXPair> : gemm_kernel<false, kNXShort>);
+    e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM), (unsigned)splits);
     e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr, xscale,

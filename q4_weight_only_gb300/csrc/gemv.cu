@@ -1043,7 +1043,7 @@ constexpr int64_t kDecodeMaxK = 65536;
 bool decode_on_tensor_cores(int64_t M, int64_t K) { return M >= 3 || K > kDecodeMaxK; }
 
 size_t gemv_workspace_bytes(int64_t M, int64_t K) {
-    return M >= 1 && M <= 32 && decode_on_tensor_cores(M, K) ? gemv_tc_workspace_bytes(M, K) : 0;
+    return M >= 1 && M <= kGemvMaxM && decode_on_tensor_cores(M, K) ? gemv_tc_workspace_bytes(M, K) : 0;
 }
 
 // The tensor-core decode puts the 128-row weight tiles in gridDim.y; the

@@ -59,12 +59,17 @@ __host__ __device__ constexpr uint32_t cols_pow2(uint32_t v) {
     return p;
 }
 
+// TM = 16 or 32: an x stage is one weight stage (256 k); TM = 64: an x
+// stage is one A slot (128 k), so that three of them and the weight ring
+// still leave room for a second CTA on the SM.
 template <int TM>
 struct Cfg {
-    static constexpr uint32_t kXAtom = TM * 128;             // [TM x 64 k] fp16, 128-byte swizzle
-    static constexpr uint32_t kXStage = kXAtom * (kKW / 64);   // one weight stage of k
-    static constexpr int kNX = TM <= 16 ? 4 : 2;                // x ring (two CTAs fit an SM)
-    static constexpr uint32_t kDCols = 32;
+    static constexpr uint32_t kXAtom = TM * 128;               // [TM x 64 k] fp16, 128-byte swizzle
+    static constexpr int kXK = TM <= 32 ? kKW : kKB;           // k per x stage
+    static constexpr int kSlotsPerX = kXK / kKB;               // A slots per x stage
+    static constexpr uint32_t kXStage = kXAtom * (kXK / 64);
+    static constexpr int kNX = TM <= 16 ? 4 : (TM <= 32 ? 2 : 3);  // x ring (two CTAs fit an SM)
+    static constexpr uint32_t kDCols = TM < 32 ? 32 : TM;
     static constexpr uint32_t kCols = cols_pow2(kDCols + kNA * (kKB / 2));
     static constexpr size_t kOffW = (size_t)kNX * kXStage;
     static constexpr size_t kOffBars = kOffW + (size_t)kNW * kWStageBytes;
@@ -285,12 +290,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 ++issued_w;
                 return true;
             };
-            auto issue_x = [&](int ws) -> bool {
-                const int xsl = ws % kNX;
-                if (!mbar_wait(&x_empty[xsl], ((ws / kNX) & 1) ^ 1, abort_flag, err)) return false;
+            // x stage xi of this CTA's K range (its tiles are contiguous in
+            // the workspace: stage u of 256 k is four 64-k atoms)
+            auto issue_x = [&](int xi) -> bool {
+                const int xsl = xi % kNX;
+                if (!mbar_wait(&x_empty[xsl], ((xi / kNX) & 1) ^ 1, abort_flag, err)) return false;
                 mbar_arrive_expect_tx(&x_full[xsl], C::kXStage);
-                bulk_g2s(xring + xsl * C::kXStage, xt + (size_t)(u0 + ws) * (C::kXStage / 16), C::kXStage,
-                         &x_full[xsl]);
+                bulk_g2s(xring + xsl * C::kXStage,
+                         xt + ((size_t)u0 * (kKW / C::kXK) + xi) * (C::kXStage / 16), C::kXStage, &x_full[xsl]);
                 ++issued_x;
                 return true;
             };
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_arrive_expect_tx(s_full, TM * 4);
             bulk_g2s(xs_smem, xscale, TM * 4, s_full);
             for (int ws = 0; ok && ws < nW; ++ws) {
-                ok = issue_x(ws);
+                for (int h = 0; ok && h < kKW / C::kXK; ++h) ok = issue_x(ws * (kKW / C::kXK) + h);
                 if (ok && ws + kNW < nW) ok = issue_w(ws + kNW);
             }
             // let every issued copy land before the CTA can exit
@@ -322,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // dequantised weights, issue its eight MMAs, release both.  x atoms of
         // 64 k are contiguous, so the descriptor's start address moves by one
         // atom every four MMAs.
+        // sub: the slot's place in its x stage
         auto slot = [&](int s, int sub, int xsl, int asl, uint32_t xpar, uint32_t apar) -> bool {
             if (sub == 0 && !__all_sync(0xffffffffu, mbar_wait(&x_full[xsl], xpar, abort_flag, err))) return false;
             if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], apar, abort_flag, err))) return false;
@@ -333,15 +341,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mma_f16_ts(d_tmem, a_tmem + asl * (kKB / 2) + kk * 8,
                                bdesc + (kk / 4) * (C::kXAtom >> 4) + 2 * (kk % 4), idesc, (s | kk) != 0);
                 mma_commit(&a_empty[asl]);
-                if (sub == kSubs - 1) mma_commit(&x_empty[xsl]);
+                if (sub == C::kSlotsPerX - 1) mma_commit(&x_empty[xsl]);
             }
             __syncwarp();
             return true;
         };
         bool ok = true;
         for (int s = 0; ok && s < nS; ++s) {
-            const int ws = s / kSubs;
-            ok = slot(s, s % kSubs, ws % kNX, s % kNA, (uint32_t)(ws / kNX) & 1u, (uint32_t)(s / kNA) & 1u);
+            const int xi = s / C::kSlotsPerX;
+            ok = slot(s, s % C::kSlotsPerX, xi % kNX, s % kNA, (uint32_t)(xi / kNX) & 1u, (uint32_t)(s / kNA) & 1u);
         }
         if (elect_one()) mma_commit(d_full);
         __syncwarp();
@@ -610,17 +618,24 @@ cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16
 
 }  // namespace
 
+namespace {
+int tile_rows_tc(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+}  // namespace
+
 size_t gemv_tc_workspace_bytes(int64_t M, int64_t K) {
     int dev = 0;
     const int sms = cudaGetDevice(&dev) == cudaSuccess ? device_sm_count(dev) : 0;
     if (sms <= 0) (void)cudaGetLastError();
-    return WorkspaceLayout(M <= 16 ? 16 : 32, K, sms > 0 ? sms : 0).bytes;
+    return WorkspaceLayout(tile_rows_tc(M), K, sms > 0 ? sms : 0).bytes;
 }
 
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                            int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
-    if (M <= 16) return launch_tm<16>(x, wq, y, ybf16, M, N, K, workspace, s, err);
-    return launch_tm<32>(x, wq, y, ybf16, M, N, K, workspace, s, err);
+    switch (tile_rows_tc(M)) {
+        case 16: return launch_tm<16>(x, wq, y, ybf16, M, N, K, workspace, s, err);
+        case 32: return launch_tm<32>(x, wq, y, ybf16, M, N, K, workspace, s, err);
+        default: return launch_tm<64>(x, wq, y, ybf16, M, N, K, workspace, s, err);
+    }
 }
 
 }  // namespace q4_0

@@ -50,9 +50,15 @@ inline float *y_offset(float *y, int64_t elems, bool ybf16) {
     return ybf16 ? reinterpret_cast<float *>(reinterpret_cast<uint16_t *>(y) + elems) : y + elems;
 }
 
-// Decode GEMV for M <= 32 (x, y point at row 0; row strides K and N).
+// Rows of x the decode kernels take (q4_0_gemv), and the largest M that
+// q4_0_matmul sends to them rather than to the GEMM.
+constexpr int64_t kGemvMaxM = 64;
+constexpr int64_t kDecodeMaxM = 64;
+
+// Decode GEMV for M <= kGemvMaxM (x, y point at row 0; row strides K and N).
 // `workspace` (256-byte aligned, gemv_workspace_bytes(M, K) bytes) is used
-// by the tensor-core decode only: 3 <= M <= 32, or M <= 2 with K > 65536.
+// by the tensor-core decode only: 3 <= M <= kGemvMaxM, or M <= 2 with
+// K > 65536.
 // gemv_shape_supported: the launch grids of the path the shape takes stay
 // within the device limits.
 size_t gemv_workspace_bytes(int64_t M, int64_t K);
@@ -71,7 +77,7 @@ cudaError_t launch_gemv_grouped(int G, const uint16_t *const *x, const uint8_t *
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
                         int64_t K, void *workspace, cudaStream_t s, unsigned int *err);
 
-// Tensor-core decode for M <= 32: x rounded once into binary16 MMA tiles in
+// Tensor-core decode for M <= 64: x rounded once into binary16 MMA tiles in
 // the workspace (gemv_tc_workspace_bytes(M, K) bytes, which also holds the
 // split-K partial tiles and counters).  N <= 65535 * 128.
 size_t gemv_tc_workspace_bytes(int64_t M, int64_t K);

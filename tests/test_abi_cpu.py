@@ -65,16 +65,19 @@ def test_workspace_sizes(lib):
     assert lib.q4_0_matmul_workspace_bytes(16, 5120, 17408) == tc(16, 17408)
     assert lib.q4_0_matmul_workspace_bytes(17, 5120, 5120) == tc(32, 5120)
     assert lib.q4_0_matmul_workspace_bytes(32, 5120, 5120) == tc(32, 5120)
-    for M in (1, 2, 3, 16, 17, 32):
+    for M in (1, 2, 3, 16, 17, 32, 33, 64):
         assert lib.q4_0_gemv_workspace_bytes(M, 5120) == lib.q4_0_matmul_workspace_bytes(M, 7, 5120)
-    assert lib.q4_0_gemv_workspace_bytes(33, 5120) == 0
+    assert lib.q4_0_matmul_workspace_bytes(33, 5120, 5120) == tc(64, 5120)
+    assert lib.q4_0_matmul_workspace_bytes(64, 5120, 5120) == tc(64, 5120)
+    assert lib.q4_0_gemv_workspace_bytes(64, 5120) == tc(64, 5120)
+    assert lib.q4_0_gemv_workspace_bytes(65, 5120) == 0
     # K % 256 != 0: zero-padded copies of W and x (256-byte aligned), then the
     # padded problem's own scratch
     assert lib.q4_0_matmul_workspace_bytes(1, 300, 96) == a256(300 * 8 * 18) + a256(1 * 256 * 2)
     assert lib.q4_0_matmul_workspace_bytes(16, 300, 5152) == (a256(300 * 168 * 18) + a256(16 * 5376 * 2)
                                                                + tc(16, 5376))
     assert lib.q4_0_matmul_workspace_bytes(64, 300, 288) >= a256(300 * 16 * 18) + a256(64 * 512 * 2) + gemm(64, 512)
-    assert lib.q4_0_matmul_workspace_bytes(33, 5120, 5120) == gemm(33, 5120)
+    assert lib.q4_0_matmul_workspace_bytes(65, 5120, 5120) == gemm(65, 5120)
     assert lib.q4_0_gemm_workspace_bytes(3, 128, 256) % 256 == 0
     # one or two rows with K past 65536 (x no longer fits shared memory) take
     # the tensor-core decode and its x tiles
@@ -94,7 +97,7 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.q4_0_gemm(good, good, good, 64, 1, 96, good, 1 << 20, None) == -2   # kernel alone: K % 256
     assert lib.q4_0_gemv_ws(good, good, good, 1, 1, 96, None, 0, None) == -2
     assert lib.q4_0_matmul(P((1 << 20) + 8), good, good, 1, 1, 256, None) == -1  # misaligned
-    assert lib.q4_0_gemv(good, good, good, 33, 1, 256, None) == -2
+    assert lib.q4_0_gemv(good, good, good, 65, 1, 256, None) == -2
     assert lib.q4_0_matmul_ex(good, good, good, 7, 1, 1, 256, None, 0, None) == -1   # unknown y type
     assert lib.q4_0_matmul_ex(good, good, good, 1, 1, 1, 48, None, 0, None) == -1    # K % 32
     assert lib.q4_0_gemv_ws(good, good, good, 16, 1, 256, None, 0, None) == -5

@@ -10,6 +10,10 @@ from q4_weight_only_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
+# q4_0_matmul sends M up to this to the decode kernels, larger M to the GEMM
+DECODE_MAX_M = 64
+
+
 def case(seed, M, N, K, outlier_blocks=0.0, act_outliers=0.0):
     w, x = synth.small_case(seed, M, N, K, outlier_block_frac=outlier_blocks,
                             act_outlier_frac=act_outliers)
@@ -23,7 +27,9 @@ SMALL_GEMV = [(1, 1, 256), (1, 2, 256), (1, 3, 512), (1, 200, 1280), (1, 257, 23
               (13, 33, 2560), (16, 512, 1024), (31, 65, 1536), (32, 256, 3072),
               # K % 1024 == 0 with M <= 2: the integer-dot decode kernel
               (1, 1, 1024), (1, 3, 2048), (1, 31, 3072), (2, 200, 1024), (2, 257, 4096),
-              (1, 1000, 7168), (2, 5, 17408), (1, 4099, 5120)]
+              (1, 1000, 7168), (2, 5, 17408), (1, 4099, 5120),
+              # 33 <= M <= 64: the tensor-core decode's 64-row tile (x stages of 128 k)
+              (33, 100, 1024), (40, 1000, 5120), (48, 300, 2048), (64, 129, 1536), (64, 5120, 17408)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALL_GEMV)
@@ -49,11 +55,11 @@ def test_gemm_small(M, N, K):
 
 def test_dispatch_matches_kernels_bitwise():
     q4 = lib()
-    for M in (1, 7, 32, 33, 200):
+    for M in (1, 7, 32, 33, 64, 65, 200):
         x, wq = case(3000 + M, M, 384, 1024)
         xd, wd = x_dev(x), wq_dev(wq)
         y = q4.matmul(xd, wd, 384, 1024)
-        ref = q4.gemv(xd, wd, 384, 1024) if M <= 32 else q4.gemm(xd, wd, 384, 1024)
+        ref = q4.gemv(xd, wd, 384, 1024) if M <= DECODE_MAX_M else q4.gemm(xd, wd, 384, 1024)
         assert torch.equal(y, ref)
         assert torch.equal(q4.matmul_alloc(xd, wd, 384, 1024), y)
 
@@ -222,7 +228,7 @@ def test_gemv_scratch_paths_agree():
     workspace, here with slack) give identical bits; a workspace one byte
     short is refused before anything is launched."""
     q4 = lib()
-    for M in (1, 3, 16, 17, 32):
+    for M in (1, 3, 16, 17, 32, 33, 64):
         x, wq = case(7100 + M, M, 300, 1536)
         xd, wd = x_dev(x), wq_dev(wq)
         a = q4.gemv(xd, wd, 300, 1536)

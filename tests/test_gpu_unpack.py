@@ -127,15 +127,15 @@ def test_one_hot_general_k_decode():
 
 @pytest.mark.parametrize("v", [1.0, -0.75])
 def test_one_hot_tensor_core_decode(v):
-    """3 <= M <= 32 through the tcgen05 batched decode: every (n, k) equals
-    RN16(w) v, for tiles of 16 and of 32 rows, and for M = 3."""
+    """3 <= M <= 64 through the tcgen05 batched decode: every (n, k) equals
+    RN16(w) v, for tiles of 16, 32 and 64 rows, and for M = 3."""
     q4 = lib()
     N, K = 300, 1024
     wq = q4_matrix(13, N, K)
     wd = wq_dev(wq)
     E = expected(wq, N, K, rounded16=True)
     X = one_hot_x(K, v)
-    for M in (3, 16, 32):
+    for M in (3, 16, 32, 64):
         rows = starts(K, M)
         Y = run_rows(lambda xs: q4.gemv(xs, wd, N, K), X, rows, N, K, M)
         assert_exact(Y, E, v, rows, M, K, f"tensor-core decode M={M}")

@@ -30,7 +30,8 @@ pytestmark = pytest.mark.gpu
 
 # (M, K, path): every kernel that takes x
 TC_PATHS = [(3, 2048, "tensor-core decode, 16-row tile"), (16, 2048, "tensor-core decode, 16-row tile"),
-            (32, 2048, "tensor-core decode, 32-row tile"), (64, 2048, "GEMM"), (512, 2048, "GEMM")]
+            (32, 2048, "tensor-core decode, 32-row tile"), (48, 2048, "tensor-core decode, 64-row tile"),
+            (96, 2048, "GEMM"), (512, 2048, "GEMM")]
 GENERAL_K = [(1, 1280, "binary16 decode"), (2, 1280, "binary16 decode")]
 INT_DOT = [(1, 2048, "integer-dot decode"), (2, 2048, "integer-dot decode")]
 N = 256
