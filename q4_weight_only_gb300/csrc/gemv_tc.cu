@@ -49,7 +49,7 @@ constexpr int kKW = 256;                  // k per weight stage
 constexpr int kSubs = kKW / kKB;          // A slots per weight stage
 constexpr int kWRowBytes = kKW / 32 * 18;  // 144
 constexpr int kWStageBytes = kTileN * kWRowBytes;
-constexpr int kNW = 3, kNA = 3;  // 32 + 3 x 64 TMEM columns <= 256
+constexpr int kNA = 3;  // A slots: D + 3 x 64 TMEM columns <= 256
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * (2 + kDequantWarps);  // 320
 
@@ -69,6 +69,7 @@ struct Cfg {
     static constexpr int kSlotsPerX = kXK / kKB;               // A slots per x stage
     static constexpr uint32_t kXStage = kXAtom * (kXK / 64);
     static constexpr int kNX = TM <= 16 ? 4 : (TM <= 32 ? 2 : 3);  // x ring (two CTAs fit an SM)
+    static constexpr int kNW = 3;  // weight ring (a fourth stage for 16- and 32-row tiles measured slower)
     static constexpr uint32_t kDCols = TM < 32 ? 32 : TM;
     static constexpr uint32_t kCols = cols_pow2(kDCols + kNA * (kKB / 2));
     static constexpr size_t kOffW = (size_t)kNX * kXStage;
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                    float *__restrict__ y, float *__restrict__ part, unsigned int *__restrict__ tile_cnt,
                    const float *__restrict__ xscale, int M, int N, int K, int ybf16, unsigned int *err) {
     using C = Cfg<TM>;
-    constexpr int kNX = C::kNX;
+    constexpr int kNX = C::kNX, kNW = C::kNW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
