@@ -106,9 +106,10 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
  * Dispatch: M <= 2 runs the decode GEMV on CUDA cores (exact integer dot
  * products per 32-weight block on 15-bit fixed-point x, fp32 across blocks;
  * a matrix whose per-row partial sums outgrow one launch's shared memory
- * runs as several launches over row ranges); 3 <= M <= 32, and M <= 2 with
+ * runs as several launches over row ranges); 3 <= M <= 64, and M <= 2 with
  * K > 65536 (x no longer fits shared memory), run the batched decode on the
- * tensor cores; M > 32 runs the tcgen05 GEMM (weights dequantised to
+ * tensor cores (tiles of 16, 32 or 64 rows of x; faster than the GEMM at
+ * every such M on a GB300); M > 64 runs the tcgen05 GEMM (weights dequantised to
  * binary16 tiles, x rounded to binary16, fp32 accumulation in tensor
  * memory).
  * Accuracy.  Inputs must be finite and y must stay within the fp32 range;
@@ -138,7 +139,7 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
  * error ||y - y_exact|| / ||y_exact|| is at most 2e-3 on the workloads' data
  * on every path (it is relative to ||y||, which cancellation can make
  * arbitrarily small, so it is a measured property, not a per-input bound).
- * Scratch: the tensor-core decode and GEMM (M > 32) paths need
+ * Scratch: the tensor-core decode and GEMM (M > 64) paths need
  * q4_0_matmul_workspace_bytes(M, N, K) bytes; this entry point takes them
  * with cudaMallocAsync on `stream` and frees them with cudaFreeAsync on the
  * same stream.  Use q4_0_matmul_ws to supply the workspace yourself.
@@ -248,9 +249,9 @@ int q4_0_matmul_grouped_launches(int G, int64_t M, const int64_t *N, const int64
 
 /*
  * q4_0_gemv -- the decode kernels alone (what q4_0_matmul runs for
- * M <= 32).  Same arguments, layout and result contract as q4_0_matmul;
- * M <= 32 (larger M is UNSUPPORTED).  M <= 2 with K <= 65536 needs no
- * scratch; on the tensor-core decode (3 <= M <= 32, or larger K) x is first
+ * M <= 64).  Same arguments, layout and result contract as q4_0_matmul;
+ * M <= 64 (larger M is UNSUPPORTED).  M <= 2 with K <= 65536 needs no
+ * scratch; on the tensor-core decode (3 <= M <= 64, or larger K) x is first
  * rounded to binary16 tensor-core tiles, and when K is split across CTAs
  * their partial tiles and counters sit beside them:
  * q4_0_gemv_workspace_bytes(M, K) bytes of scratch, which this entry point
@@ -259,7 +260,7 @@ int q4_0_matmul_grouped_launches(int G, int64_t M, const int64_t *N, const int64
 int q4_0_gemv(const uint16_t *x, const uint8_t *wq, float *y,
               int64_t M, int64_t N, int64_t K, void *stream);
 
-/* Scratch bytes of the decode kernels on the current device (0 for M > 32,
+/* Scratch bytes of the decode kernels on the current device (0 for M > 64,
  * and for M <= 2 with K <= 65536): the binary16 x tiles plus room for two
  * split-K partial tiles (and counters) per SM, whatever N is. */
 size_t q4_0_gemv_workspace_bytes(int64_t M, int64_t K);
@@ -277,7 +278,7 @@ int q4_0_gemv_ws(const uint16_t *x, const uint8_t *wq, float *y,
 
 /*
  * q4_0_gemm -- the tcgen05 prefill kernel alone (what q4_0_matmul runs for
- * M > 32), usable at any M >= 1 for cross-checks.  Workspace as in
+ * M > 64), usable at any M >= 1 for cross-checks.  Workspace as in
  * q4_0_matmul_ws: q4_0_gemm_workspace_bytes(M, N, K) bytes on the current
  * device -- x rounded to binary16 and, when the output tiles alone would
  * leave SMs idle, fp32 partial tiles of a 2- to 4-way split of K (summed

@@ -446,3 +446,21 @@ def test_prefill_down_m512_every_output():
     y = q4.matmul(x_dev(x), wq_dev(wq), N, K)
     check_full(y, x, wq, N, K)
     assert q4.device_error() == 0
+
+
+@pytest.mark.parametrize("M,K", [(256, 1024), (128, 512)])
+def test_gemm_whole_waves_and_a_ragged_wave(M, K):
+    """More output tiles than CTA slots, the last wave only partly full:
+    256-row tiles give one slot per SM, 128-row tiles two (paired CTAs with
+    the shallow x ring).  Every output against the oracle, and the result
+    repeats bit for bit."""
+    q4 = lib()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    slots = sms * (2 if M <= 128 else 1)
+    N = 128 * (slots + 20)                      # one whole wave, then 20 tiles
+    x, wq = case(9500 + M, M, N, K, outlier_blocks=0.05, act_outliers=0.01)
+    xd, wd = x_dev(x), wq_dev(wq)
+    y = q4.gemm(xd, wd, N, K)
+    check_full(y, x, wq, N, K)
+    assert torch.equal(q4.gemm(xd, wd, N, K), y)
+    assert q4.device_error() == 0
