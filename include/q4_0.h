@@ -146,8 +146,7 @@ int q4_0_quantize(const float *w, uint8_t *wq, int64_t N, int64_t K, void *strea
  * Alignment: x, wq and y 16 bytes.
  * Sizes this build runs (else UNSUPPORTED): M, N <= 2^30, K <= 2^24, each of
  * M*K, N*K, M*N <= 2^40; on the tensor-core decode N <= 65535 * 128 (its
- * weight tiles are a grid dimension); on the GEMM at most 65535 x tiles
- * (M up to about 16.7 million rows).
+ * weight tiles are a grid dimension).
  * Returns Q4_0_OK, Q4_0_ERR_INVALID_ARG, Q4_0_ERR_UNSUPPORTED or Q4_0_ERR_CUDA.
  */
 int q4_0_matmul(const uint16_t *x, const uint8_t *wq, float *y,

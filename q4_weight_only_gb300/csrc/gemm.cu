@@ -53,6 +53,8 @@ constexpr int kNXShort = 5, kNXTall = 4;
 // which bind the GEMM at small M) only with a three-stage x ring; up to 80
 // rows five stages fit beside a second CTA.
 constexpr int kNXPair = 3, kPairMaxRows = 128;
+// x tiles per band of the tile order (see gemm_kernel)
+constexpr int kBandMTiles = 8;
 constexpr int kMaxTileRows = 320;
 constexpr int kThreads = 192;
 
@@ -256,7 +258,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *xs_tile = reinterpret_cast<float *>(smem + Cfg.scale_off);  // [TM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * TM;
+    // tile order: bands of up to kBandMTiles x tiles; within a band, the x
+    // tiles of one weight tile are neighbours, so a weight tile comes from
+    // HBM once per band while the band's x rows stay in L2
+    const int NT = (N + kTileN - 1) / kTileN, MT = (M + TM - 1) / TM;
+    int n0, m0;
+    {
+        const int64_t b = blockIdx.x;
+        const int64_t per_band = (int64_t)NT * kBandMTiles;
+        const int bands = (MT + kBandMTiles - 1) / kBandMTiles;
+        const int band = (int)(b / per_band < bands - 1 ? b / per_band : bands - 1);
+        const int64_t r = b - (int64_t)band * per_band;
+        const int gm = MT - band * kBandMTiles < kBandMTiles ? MT - band * kBandMTiles : kBandMTiles;
+        n0 = (int)(r / gm) * kTileN;
+        m0 = (band * kBandMTiles + (int)(r % gm)) * TM;
+    }
     // split-K: CTA z of gridDim.z takes weight stages [w_begin, w_end) and,
     // when split, writes its partial tile to part[z] instead of y
     const int KW_all = K / kKW;
@@ -533,7 +549,7 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
                        : (nx == kNXPair ? gemm_kernel<false, kNXPair> : gemm_kernel<false, kNXShort>);
     e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + TM - 1) / TM), (unsigned)splits);
+    const dim3 grid((unsigned)(((N + kTileN - 1) / kTileN) * ((M + TM - 1) / TM)), 1, (unsigned)splits);
     e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr, xscale,
                    (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
     if (e != cudaSuccess || splits == 1) return e;
@@ -586,12 +602,12 @@ int gemm_splits(int64_t M, int64_t N, int64_t K, int sms) {
     return best;
 }
 
-// The launch grids: M tiles in gridDim.y (at most 65535), N tiles in
-// gridDim.x, and the x pre-pass at one CTA per row of x.
+// The launch grids: all output tiles in gridDim.x, and the x pre-pass at
+// one CTA per row of x.
 bool gemm_shape_supported(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 1) return false;
     const int tm = tile_rows(M);
-    return (M + tm - 1) / tm <= 65535 && (N + kTileN - 1) / kTileN <= 0x7FFFFFFF && M <= 0x7FFFFFFF;
+    return ((N + kTileN - 1) / kTileN) * ((M + tm - 1) / tm) <= 0x7FFFFFFF && M <= 0x7FFFFFFF;
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {

@@ -112,15 +112,16 @@ def test_invalid_arguments_rejected_before_cuda(lib):
 
 def test_shapes_past_the_grid_limits_are_unsupported(lib):
     """Shapes the launch grids cannot hold are refused before any CUDA call:
-    the tensor-core decode's weight tiles (N <= 65535 * 128) and the GEMM's
-    x tiles (at most 65535)."""
+    the tensor-core decode's weight tiles (N <= 65535 * 128), and sizes past
+    the caps (M, N <= 2^30; the GEMM's one-dimensional grid of tiles then
+    always fits)."""
     good = ctypes.c_void_p(1 << 20)
     ws = ctypes.c_void_p(1 << 21)
     assert lib.q4_0_matmul_ws(good, good, good, 16, 65535 * 128 + 1, 256, ws, 1 << 40, None) == -2
     assert lib.q4_0_matmul_ws(good, good, good, 1, 65535 * 128 + 1, 65792, ws, 1 << 40, None) == -2
-    assert lib.q4_0_matmul_ws(good, good, good, 1 << 25, 128, 256, ws, 1 << 40, None) == -2
     assert lib.q4_0_gemv_ws(good, good, good, 16, 65535 * 128 + 1, 256, ws, 1 << 40, None) == -2
-    assert lib.q4_0_gemm(good, good, good, 1 << 25, 128, 256, ws, 1 << 40, None) == -2
+    assert lib.q4_0_gemm(good, good, good, (1 << 30) + 1, 128, 256, ws, 1 << 40, None) == -2
+    assert lib.q4_0_matmul_ws(good, good, good, (1 << 30) + 1, 128, 256, ws, 1 << 40, None) == -2
 
 
 def test_grouped_validates_every_problem_before_any_launch(lib):
