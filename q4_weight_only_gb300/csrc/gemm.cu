@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <mutex>
+#include <type_traits>
 
 #include "q4_0_internal.h"
 #include "q4_0_ptx.cuh"
@@ -205,14 +206,20 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__rest
 // One 32-bit word of codes yields its bytes 0 and 2 (or 1 and 3) as a pair, so
 // within every aligned group of four elements the pair order is (0, 2), (1, 3):
 // k positions 1 and 2 of each group are swapped, and the x operand carries the
-// same swap (swap_mid_pairs).  d / 16 is exact for |d| >= 2^-10; smaller scales
-// shift the high nibbles down and use the 1032 route for them too.  The shift
-// by a byte is a high multiply, which runs on the FMA pipe rather than the ALU.
+// same swap (swap_mid_pairs).  The shift by a byte is a high multiply, which
+// runs on the FMA pipe rather than the ALU.
+// kAnyScale false: d / 16 must be exact, i.e. |d| >= 2^-10 (scale_is_large);
+// true: the high nibbles are shifted down and take the 1032 route too, which
+// holds for every scale (subnormal and zero included) at two more
+// instructions per word.  Both give the same bits.
+__device__ __forceinline__ bool scale_is_large(uint32_t dbits) { return (dbits & 0x7C00u) >= 0x1400u; }
+
+template <bool kAnyScale>
 __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q)[4], uint32_t *out) {
     const uint32_t kBias = 0x64006400u;                         // (1024, 1024)
     const half2 k1032 = u2h(0x64086408u), k1152 = u2h(0x64806480u);
     const half2 d2 = u2h(dbits * 0x00010001u);                  // (d, d)
-    if ((dbits & 0x7C00u) >= 0x1400u) {                         // |d| >= 2^-10
+    if (!kAnyScale) {
         const half2 d16 = __hmul2(d2, u2h(0x2C002C00u));         // d / 16, exact
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
@@ -412,28 +419,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rw[4 * i + 2] = q.z;
                 rw[4 * i + 3] = q.w;
             }
+            // the route is chosen once for the warp's eight blocks of the
+            // stage: a branch per block cost about a tenth of the rate
+            bool large = true;
 #pragma unroll
-            for (int sub = 0; sub < kKW / kKB; ++sub) {
-                const int s = ws * (kKW / kKB) + sub, asl = s % kNA;
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t *wv = rw + 9 * sub;
-                const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16),
-                                        __funnelshift_r(wv[1], wv[2], 16),
-                                        __funnelshift_r(wv[2], wv[3], 16),
-                                        __funnelshift_r(wv[3], wv[4], 16)};
-                const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
-                uint32_t cols[32];
-                dequant_block(wv[0] & 0xFFFFu, Q0, cols);
-                dequant_block(wv[4] >> 16, Q1, cols + 16);
-                tmem_st32(a_tmem + lane_base + asl * 32, cols);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();  // every lane's stores are done
-                if (lane == 0) mbar_arrive(&a_full[asl]);
-            }
+            for (int sub = 0; sub < kKW / kKB; ++sub)
+                large = large && scale_is_large(rw[9 * sub] & 0xFFFFu) && scale_is_large(rw[9 * sub + 4] >> 16);
+            auto stage_subs = [&](auto any_c) {
+                constexpr bool kAny = decltype(any_c)::value;
+#pragma unroll
+                for (int sub = 0; sub < kKW / kKB; ++sub) {
+                    const int s = ws * (kKW / kKB) + sub, asl = s % kNA;
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t *wv = rw + 9 * sub;
+                    const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16),
+                                            __funnelshift_r(wv[1], wv[2], 16),
+                                            __funnelshift_r(wv[2], wv[3], 16),
+                                            __funnelshift_r(wv[3], wv[4], 16)};
+                    const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+                    uint32_t cols[32];
+                    dequant_block<kAny>(wv[0] & 0xFFFFu, Q0, cols);
+                    dequant_block<kAny>(wv[4] >> 16, Q1, cols + 16);
+                    tmem_st32(a_tmem + lane_base + asl * 32, cols);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();  // every lane's stores are done
+                    if (lane == 0) mbar_arrive(&a_full[asl]);
+                }
+            };
+            if (__all_sync(0xffffffffu, large))
+                stage_subs(std::integral_constant<bool, false>{});
+            else
+                stage_subs(std::integral_constant<bool, true>{});
             if (lane == 0) mbar_arrive(&w_empty[wsl]);
         }
         // epilogue: D[row r][column m] -> y[m][n0 + r], times the x row's

@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 #include <mutex>
 #include <type_traits>
+#include <type_traits>
 
 #include "q4_0_internal.h"
 #include "q4_0_ptx.cuh"
@@ -90,14 +91,20 @@ __device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint
 // One 32-bit word of codes yields its bytes 0 and 2 (or 1 and 3) as a pair, so
 // within every aligned group of four elements the pair order is (0, 2), (1, 3):
 // k positions 1 and 2 of each group are swapped, and the x operand carries the
-// same swap (swap_mid_pairs).  d / 16 is exact for |d| >= 2^-10; smaller scales
-// shift the high nibbles down and use the 1032 route for them too.  The shift
-// by a byte is a high multiply, which runs on the FMA pipe rather than the ALU.
+// same swap (swap_mid_pairs).  The shift by a byte is a high multiply, which
+// runs on the FMA pipe rather than the ALU.
+// kAnyScale false: d / 16 must be exact, i.e. |d| >= 2^-10 (scale_is_large);
+// true: the high nibbles are shifted down and take the 1032 route too, which
+// holds for every scale (subnormal and zero included) at two more
+// instructions per word.  Both give the same bits.
+__device__ __forceinline__ bool scale_is_large(uint32_t dbits) { return (dbits & 0x7C00u) >= 0x1400u; }
+
+template <bool kAnyScale>
 __device__ __forceinline__ void dequant_block16(uint32_t dbits, const uint32_t (&Q)[4], uint32_t (&out)[16]) {
     const uint32_t kBias = 0x64006400u;                         // (1024, 1024)
     const half2 k1032 = u2h(0x64086408u), k1152 = u2h(0x64806480u);
     const half2 d2 = u2h(dbits * 0x00010001u);                  // (d, d)
-    if ((dbits & 0x7C00u) >= 0x1400u) {                         // |d| >= 2^-10
+    if (!kAnyScale) {
         const half2 d16 = __hmul2(d2, u2h(0x2C002C00u));         // d / 16, exact
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
@@ -390,19 +397,30 @@ __global__ void __launch_bounds__(kThreads, 2)
                 // A slot (stage, half): 128 k = two 64-k pieces of 32 columns
                 if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[asl], aph ^ 1, abort_flag, err))) return false;
                 tc_fence_after();
+                // the route is chosen once for the warp's four blocks of the
+                // stage: a branch per block cost about a tenth of the rate
+                const bool large = scale_is_large(rw[2 * H] & 0xFFFFu) && scale_is_large(rw[2 * H + 4] >> 16) &&
+                                   scale_is_large(rw[2 * H + 9] & 0xFFFFu) && scale_is_large(rw[2 * H + 13] >> 16);
+                auto slot_pieces = [&](auto any_c) {
+                    constexpr bool kAny = decltype(any_c)::value;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t *wv = rw + 2 * H + 9 * j;
-                    const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
-                                            __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
-                    const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
-                    uint32_t cols[32];
-                    uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols);
-                    uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols + 16);
-                    dequant_block16(wv[0] & 0xFFFFu, Q0, lo);
-                    dequant_block16(wv[4] >> 16, Q1, hi);
-                    tmem_st32(a_tmem + lane_base + asl * (kKB / 2) + j * 32, cols);
-                }
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t *wv = rw + 2 * H + 9 * j;
+                        const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
+                                                __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
+                        const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+                        uint32_t cols[32];
+                        uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols);
+                        uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols + 16);
+                        dequant_block16<kAny>(wv[0] & 0xFFFFu, Q0, lo);
+                        dequant_block16<kAny>(wv[4] >> 16, Q1, hi);
+                        tmem_st32(a_tmem + lane_base + asl * (kKB / 2) + j * 32, cols);
+                    }
+                };
+                if (__all_sync(0xffffffffu, large))
+                    slot_pieces(std::integral_constant<bool, false>{});
+                else
+                    slot_pieces(std::integral_constant<bool, true>{});
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();  // every lane's stores are done

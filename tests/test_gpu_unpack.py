@@ -20,7 +20,10 @@ The expected values come from the oracle alone: its dequantize (w, exact in
 fp64) and its binary16 encoder (RN16), both pinned against IEEE 754.  The
 matrices mix every scale class the kernels treat differently: |d| >= 2^-10
 (the d / 16 route), normal |d| < 2^-10 and subnormal d (the shift route),
-d = 0, and |d| >= 64; both signs; every code value.
+d = 0, and |d| >= 64; both signs; every code value.  Rows in alternate
+128-row weight tiles hold large scales only, so that both the stages taken
+through the d / 16 route and the mixed stages taken through the shift route
+are checked.
 """
 import numpy as np
 import pytest
@@ -38,6 +41,12 @@ def q4_matrix(seed, N, K):
     rng = np.random.default_rng(seed)
     nb = K // 32
     cls = rng.integers(0, 5, size=(N, nb))
+    # the tensor-core kernels pick the d / 16 route for a whole stage of a
+    # warp's 32 rows when every scale in it is large: rows in even 128-row
+    # tiles draw large scales only, so that route is taken there, and the
+    # odd tiles mix all five classes
+    large_only = (np.arange(N) // 128 % 2 == 0)[:, None]
+    cls = np.where(large_only, np.where(rng.random((N, nb)) < 0.5, 0, 4), cls)
     exp = np.select([cls == 0, cls == 1, cls == 4], [rng.integers(5, 15, size=(N, nb)),
                                                       rng.integers(1, 5, size=(N, nb)),
                                                       rng.integers(21, 27, size=(N, nb))], 0)
