@@ -1,4 +1,4 @@
-// gemv_tc.cu -- batched decode (3 <= M <= 32) on the 5th-generation tensor
+// gemv_tc.cu -- batched decode (3 <= M <= 64) on the 5th-generation tensor
 // cores.
 //
 // "Vertical disaggregation: maximizing model throughput on heterogeneous
@@ -19,8 +19,8 @@
 //     stage's x tile with one bulk copy.  Converting inside every CTA would
 //     repeat the same work once per weight tile and load the schedulers of
 //     two SM quarters more than the others;
-//   * D = 128 x TM fp32 in tensor memory (TM = 16 or 32, padded rows of x are
-//     zero);
+//   * D = 128 x TM fp32 in tensor memory (TM = 16, 32 or 64, padded rows of x
+//     are zero);
 //   * N is tiled by 128 rows; when the tiles alone leave SMs idle, K is
 //     split over S CTAs per tile, each streaming its K range once.  They
 //     write their fp32 partial tiles to the workspace and count themselves
@@ -35,7 +35,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <mutex>
-#include <type_traits>
 #include <type_traits>
 
 #include "q4_0_internal.h"
