@@ -367,44 +367,38 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int quad = warp & 3, half = (warp - 2) >> 2;
         const int r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        // the half is a compile-time constant inside the loop (one copy per
-        // half, chosen per warp), so register indices stay static without
-        // selects; ring slots and phases advance incrementally (A slot
-        // s = 2 ws + half steps by two through a ring of three)
-        auto dequant = [&](auto half_c) -> bool {
-            constexpr int H = decltype(half_c)::value;
-            int wsl = 0, asl = H;
+        // ring slots and phases advance incrementally (A slot s = 2 ws + half
+        // steps by two through a ring of three)
+        auto dequant = [&]() -> bool {
+            int wsl = 0, asl = half;
             uint32_t wph = 0, aph = 0;
             for (int ws = 0; ws < nW; ++ws) {
                 if (!__all_sync(0xffffffffu, mbar_wait(&w_full[wsl], wph, abort_flag, err))) return false;
-                // this warp's half of the row (bytes 72h .. 72h + 71) with five
-                // 16-byte loads from byte 64h: a 144-byte row stride puts the
-                // eight lanes of each load phase on distinct 16-byte bank groups,
-                // where 4-byte loads would conflict four ways; half 1 skips the
-                // first two words
-                const uint4 *row =
-                    reinterpret_cast<const uint4 *>(wring + wsl * kWStageBytes + r * kWRowBytes + 64 * H);
-                uint32_t rw[20];
+                // this warp's half of the row (bytes 72h .. 72h + 71) with nine
+                // 8-byte loads: with a 144-byte row stride each load costs two
+                // shared-memory wavefronts, as many as the 16-byte loads of the
+                // same bytes would, and both halves run the same code
+                const uint2 *row =
+                    reinterpret_cast<const uint2 *>(wring + wsl * kWStageBytes + r * kWRowBytes + 72 * half);
+                uint32_t rw[18];
 #pragma unroll
-                for (int i = 0; i < 5; ++i) {
-                    const uint4 q = row[i];
-                    rw[4 * i + 0] = q.x;
-                    rw[4 * i + 1] = q.y;
-                    rw[4 * i + 2] = q.z;
-                    rw[4 * i + 3] = q.w;
+                for (int i = 0; i < 9; ++i) {
+                    const uint2 q = row[i];
+                    rw[2 * i + 0] = q.x;
+                    rw[2 * i + 1] = q.y;
                 }
                 // A slot (stage, half): 128 k = two 64-k pieces of 32 columns
                 if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[asl], aph ^ 1, abort_flag, err))) return false;
                 tc_fence_after();
                 // the route is chosen once for the warp's four blocks of the
                 // stage: a branch per block cost about a tenth of the rate
-                const bool large = scale_is_large(rw[2 * H] & 0xFFFFu) && scale_is_large(rw[2 * H + 4] >> 16) &&
-                                   scale_is_large(rw[2 * H + 9] & 0xFFFFu) && scale_is_large(rw[2 * H + 13] >> 16);
+                const bool large = scale_is_large(rw[0] & 0xFFFFu) && scale_is_large(rw[4] >> 16) &&
+                                   scale_is_large(rw[9] & 0xFFFFu) && scale_is_large(rw[13] >> 16);
                 auto slot_pieces = [&](auto any_c) {
                     constexpr bool kAny = decltype(any_c)::value;
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const uint32_t *wv = rw + 2 * H + 9 * j;
+                        const uint32_t *wv = rw + 9 * j;
                         const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16), __funnelshift_r(wv[1], wv[2], 16),
                                                 __funnelshift_r(wv[2], wv[3], 16), __funnelshift_r(wv[3], wv[4], 16)};
                         const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
@@ -445,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             return true;
         };
         static_assert(kSubs < kNA, "the A slot advances by kSubs and wraps at most once per stage");
-        bool ok = half ? dequant(std::integral_constant<int, 1>{}) : dequant(std::integral_constant<int, 0>{});
+        bool ok = dequant();
         // epilogue (warps 2..5 cover the four lane quarters): D -> partial tile
         if (half == 0) {
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(d_full, 0, abort_flag, err));
