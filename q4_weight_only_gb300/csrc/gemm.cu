@@ -57,7 +57,12 @@ constexpr int kNXPair = 3, kPairMaxRows = 128;
 // x tiles per band of the tile order (see gemm_kernel)
 constexpr int kBandMTiles = 8;
 constexpr int kMaxTileRows = 320;
-constexpr int kThreads = 192;
+// warp 0: weight copies; warp 1: MMA issue; warps 2-5: dequantisation and
+// the epilogue; warp 6: x copies.  A bulk tensor copy holds its issuing thread
+// for about 0.15 us, so one thread issuing both streams (five copies per
+// weight stage, nine for a tall tile) fell behind the MMAs.
+constexpr int kThreads = 224;
+constexpr int kXProducerWarp = 6;
 
 __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
     uint32_t p = 32;
@@ -320,37 +325,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // producer: weight stage ws, then its four x stages
-            int issued_w = 0, issued_x = 0;
+            // weight stages
+            int issued_w = 0;
             for (int ws = 0; ws < KWS; ++ws) {
                 const int wsl = ws % kNW;
                 if (!mbar_wait(&w_empty[wsl], ((ws / kNW) & 1) ^ 1, abort_flag, err)) break;
                 mbar_arrive_expect_tx(&w_full[wsl], kWStageBytes);
                 tma_load_2d(wring + wsl * kWStageBytes, &wmap, (w_begin + ws) * kWRowBytes, n0, &w_full[wsl]);
                 ++issued_w;
-                bool ok = true;
-                for (int sub = 0; sub < kKW / kKB; ++sub) {
-                    const int s = ws * (kKW / kKB) + sub, xsl = s % kNX;
-                    if (!mbar_wait(&x_empty[xsl], ((s / kNX) & 1) ^ 1, abort_flag, err)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
-                    const int kx = w_begin * (kKW / kKB) * kKB + s * kKB;
-                    if (!kTall) {
-                        tma_load_2d(xring + xsl * Cfg.x_stage, &xmap, kx, m0, &x_full[xsl]);
-                    } else {  // a TMA box is at most 256 rows: two boxes of TM / 2
-                        tma_load_2d(xring + xsl * Cfg.x_stage, &xmap, kx, m0, &x_full[xsl]);
-                        tma_load_2d(xring + xsl * Cfg.x_stage + (TM / 2) * 128, &xmap, kx, m0 + TM / 2,
-                                    &x_full[xsl]);
-                    }
-                    ++issued_x;
-                }
-                if (!ok) break;
             }
             // let every issued copy land before the CTA can exit
             for (int i = issued_w - kNW; i < issued_w; ++i)
                 if (i >= 0) mbar_drain(&w_full[i % kNW], (i / kNW) & 1);
+        }
+    } else if (warp == kXProducerWarp) {
+        if (lane == 0) {
+            // x stages (64 k each)
+            int issued_x = 0;
+            for (int s = 0; s < KS; ++s) {
+                const int xsl = s % kNX;
+                if (!mbar_wait(&x_empty[xsl], ((s / kNX) & 1) ^ 1, abort_flag, err)) break;
+                mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
+                const int kx = w_begin * (kKW / kKB) * kKB + s * kKB;
+                tma_load_2d(xring + xsl * Cfg.x_stage, &xmap, kx, m0, &x_full[xsl]);
+                if (kTall)  // a TMA box is at most 256 rows: two boxes of TM / 2
+                    tma_load_2d(xring + xsl * Cfg.x_stage + (TM / 2) * 128, &xmap, kx, m0 + TM / 2, &x_full[xsl]);
+                ++issued_x;
+            }
             for (int i = issued_x - kNX; i < issued_x; ++i)
                 if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
         }
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (elect_one()) mma_commit(d_full);
         __syncwarp();
-    } else {
+    } else if (warp >= 2 && warp < 6) {
         // warps 2..5: dequantise into TMEM, then the epilogue
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // weight row within the tile
