@@ -41,15 +41,25 @@ namespace q4_0 {
 namespace {
 
 constexpr int kTileN = 128;                 // weight rows per CTA (MMA M)
-constexpr int kKB = 64;                     // k per MMA stage
 constexpr int kKW = 256;                    // k per weight stage
 constexpr int kWRowBytes = kKW / 32 * 18;   // 144
 constexpr int kWStageBytes = kTileN * kWRowBytes;
-constexpr int kNW = 3, kNA = 4;              // weight and A-slot ring depths
-// x ring depth: five stages for tiles of up to 256 rows (an x stage is
-// 32 KB there, and L2 latency under the stream needs the depth); a tall tile
-// (up to kMaxTileRows rows, 40 KB a stage) fits four
-constexpr int kNXShort = 5, kNXTall = 4;
+constexpr int kNW = 3;                      // weight ring depth
+// A slot and x stage: 128 k for tiles of 129..192 rows and tall tiles, 64 k
+// otherwise.  Every slot costs the MMA warp two barrier waits, two commits
+// and a fence, about as long as the four MMAs of a 64-k slot for 256 x rows;
+// a 128-k slot (eight MMAs) leaves the tensor pipe the longer of the two.
+// Tiles of 193..256 rows keep 64 k: two 128-k stages of x (all that fits)
+// hold less x in flight than five 64-k ones, and measured slower.  Small
+// tiles keep 64 k too (their CTAs pair up on an SM, which halves the tensor
+// memory and shared memory a CTA may hold).
+constexpr int kWideSlotMinRows = 129, kWideSlotMaxRows = 192;
+constexpr int kMaxTileRowsShort = 256;      // one MMA wide; taller tiles take a second MMA
+constexpr int kNAMax = 4;                   // A slots at most (fewer where tensor memory is short)
+// x ring depth: two 128-k stages for tall tiles (up to 80 KB a stage), three
+// for 129..192 rows (up to 48 KB); five 64-k stages for tiles of 193..256
+// rows (32 KB) and for small tiles alone on an SM
+constexpr int kNXShort = 5, kNXMid = 3, kNXTall = 2;
 // Tiles of 96..128 rows keep two CTAs on an SM (twice the dequantising warps,
 // which bind the GEMM at small M) only with a three-stage x ring; up to 80
 // rows five stages fit beside a second CTA.
@@ -58,10 +68,11 @@ constexpr int kNXPair = 3, kPairMaxRows = 128;
 constexpr int kBandMTiles = 8;
 constexpr int kMaxTileRows = 320;
 // warp 0: weight copies; warp 1: MMA issue; warps 2-5: dequantisation and
-// the epilogue; warp 6: x copies.  A bulk tensor copy holds its issuing thread
-// for about 0.15 us, so one thread issuing both streams (five copies per
-// weight stage, nine for a tall tile) fell behind the MMAs.
-constexpr int kThreads = 224;
+// the epilogue; warps 6 and 7: x copies (even and odd stages of an even
+// ring; an odd ring has one producer).  Issuing a bulk tensor copy holds the
+// thread for about 0.15 us, so one thread issuing every copy fell behind the
+// MMAs.
+constexpr int kThreads = 256;
 constexpr int kXProducerWarp = 6;
 
 __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
@@ -70,17 +81,28 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
     return p;
 }
 
-// Shared-memory and TMEM layout of a CTA for an x tile of `tm` rows.
+// k per A slot and x stage for a tile of tm rows.
+__host__ __device__ constexpr int slot_k(int tm) {
+    return tm > kMaxTileRowsShort || (tm >= kWideSlotMinRows && tm <= kWideSlotMaxRows) ? 128 : 64;
+}
+
+// Shared-memory and TMEM layout of a CTA for an x tile of `tm` rows: an x
+// stage is slot_k / 64 chunks of [tm rows x 64 k] (128-byte rows, the MMA's
+// 128-byte swizzle); an A slot slot_k / 2 TMEM columns.  Tiles of up to 128
+// rows keep to 256 columns (two CTAs may share the SM's 512).
 struct GemmLayout {
     uint32_t x_stage, d_cols, cols;
     size_t bar_off, scale_off, smem;
-    int num_bars;
+    int num_bars, na;
     __host__ __device__ GemmLayout(int tm, int nx) {
-        x_stage = (uint32_t)tm * 128;
+        const int sk = slot_k(tm);
+        x_stage = (uint32_t)tm * 2 * sk;
         d_cols = tm < 32 ? 32 : (uint32_t)((tm + 31) / 32 * 32);
-        cols = pow2_at_least(d_cols + kNA * 32);
+        const int budget = d_cols <= 128 ? 256 : 512;
+        na = (budget - (int)d_cols) / (sk / 2) < kNAMax ? (budget - (int)d_cols) / (sk / 2) : kNAMax;
+        cols = pow2_at_least(d_cols + na * (sk / 2));
         bar_off = (size_t)nx * x_stage + (size_t)kNW * kWStageBytes;
-        num_bars = 2 * kNW + 2 * nx + 2 * kNA + 2;
+        num_bars = 2 * kNW + 2 * nx + 2 * kNAMax + 2;
         scale_off = bar_off + num_bars * 8 + 16;  // the tile's x-row scales (tm rounded up to 32 floats)
         smem = 1024 + scale_off + (size_t)((tm + 31) / 32 * 32) * 4;
     }
@@ -91,7 +113,9 @@ struct GemmLayout {
 // (shared memory and tensor memory both fit two) and there are more CTAs
 // than SMs to pair up; a CTA alone on its SM keeps the deep ring.
 int x_ring_stages(int tm, int64_t ctas, int sms) {
-    if (tm > 256) return kNXTall;
+    if (tm > kMaxTileRowsShort) return kNXTall;
+    if (tm > kWideSlotMaxRows) return kNXShort;
+    if (tm >= kWideSlotMinRows) return kNXMid;
     if (tm > 80 && tm <= kPairMaxRows && ctas > sms) return kNXPair;
     return kNXShort;
 }
@@ -246,15 +270,19 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
     }
 }
 
-// kTall: x tiles of more than 256 rows (two TMA boxes per x stage, a second
+// kTall: x tiles of more than 256 rows (two TMA boxes per x chunk, a second
 // MMA per k step); a separate instantiation keeps the common path unchanged.
-// kNX: stages of the x ring.
-template <bool kTall, int kNX>
+// kNX: stages of the x ring.  kSK: k per A slot and x stage (slot_k(TM)).
+template <bool kTall, int kNX, int kSK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 float *__restrict__ y, float *__restrict__ part, const float *__restrict__ xscale, int M, int N,
                 int K, int TM, int ybf16, unsigned int *err) {
+    constexpr int kChunks = kSK / 64;         // 64-k pieces per slot (x TMA boxes, A stores)
+    constexpr int kSlotsPerW = kKW / kSK;     // A slots per weight stage
+    constexpr int kSlotCols = kSK / 2;        // TMEM columns per A slot
     const GemmLayout Cfg(TM, kNX);
+    const int na = Cfg.na;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -263,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg.bar_off);
     uint64_t *w_full = bars, *w_empty = bars + kNW;
     uint64_t *x_full = bars + 2 * kNW, *x_empty = x_full + kNX;
-    uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNA;
-    uint64_t *d_full = a_empty + kNA, *drain = d_full + 1;
+    uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNAMax;
+    uint64_t *d_full = a_empty + kNAMax, *drain = d_full + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg.num_bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *xs_tile = reinterpret_cast<float *>(smem + Cfg.scale_off);  // [TM]
@@ -290,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int KW_all = K / kKW;
     const int w_begin = (int)((int64_t)blockIdx.z * KW_all / gridDim.z);
     const int w_end = (int)((int64_t)(blockIdx.z + 1) * KW_all / gridDim.z);
-    const int KWS = w_end - w_begin, KS = KWS * (kKW / kKB);
+    const int KWS = w_end - w_begin, KS = KWS * kSlotsPerW;
     float *out = part ? part + (size_t)blockIdx.z * M * N : nullptr;  // fp32 partial tile of a K split
 
     if (threadIdx.x == 0) {
@@ -302,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&x_full[i], 1);
             mbar_init(&x_empty[i], 1);
         }
-        for (int i = 0; i < kNA; ++i) {
+        for (int i = 0; i < na; ++i) {
             mbar_init(&a_full[i], 4);
             mbar_init(&a_empty[i], 1);
         }
@@ -338,21 +366,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = issued_w - kNW; i < issued_w; ++i)
                 if (i >= 0) mbar_drain(&w_full[i % kNW], (i / kNW) & 1);
         }
-    } else if (warp == kXProducerWarp) {
-        if (lane == 0) {
-            // x stages (64 k each)
-            int issued_x = 0;
-            for (int s = 0; s < KS; ++s) {
+    } else if (warp == kXProducerWarp || warp == kXProducerWarp + 1) {
+        // x stages: producer p takes stages p, p + P, ... (with an even ring
+        // each producer owns its slots, so their phases follow in order)
+        constexpr int P = kNX % 2 == 0 ? 2 : 1;
+        const int p = warp - kXProducerWarp;
+        if (lane == 0 && p < P) {
+            int next = p;  // first stage not issued
+            for (int s = p; s < KS; s += P) {
                 const int xsl = s % kNX;
                 if (!mbar_wait(&x_empty[xsl], ((s / kNX) & 1) ^ 1, abort_flag, err)) break;
                 mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
-                const int kx = w_begin * (kKW / kKB) * kKB + s * kKB;
-                tma_load_2d(xring + xsl * Cfg.x_stage, &xmap, kx, m0, &x_full[xsl]);
-                if (kTall)  // a TMA box is at most 256 rows: two boxes of TM / 2
-                    tma_load_2d(xring + xsl * Cfg.x_stage + (TM / 2) * 128, &xmap, kx, m0 + TM / 2, &x_full[xsl]);
-                ++issued_x;
+                uint8_t *dst = xring + xsl * Cfg.x_stage;
+#pragma unroll
+                for (int j = 0; j < kChunks; ++j) {
+                    const int kx = w_begin * kKW + s * kSK + 64 * j;
+                    tma_load_2d(dst + j * TM * 128, &xmap, kx, m0, &x_full[xsl]);
+                    if (kTall)  // a TMA box is at most 256 rows: two boxes of TM / 2
+                        tma_load_2d(dst + j * TM * 128 + (TM / 2) * 128, &xmap, kx, m0 + TM / 2, &x_full[xsl]);
+                }
+                next = s + P;
             }
-            for (int i = issued_x - kNX; i < issued_x; ++i)
+            // let this producer's copies land before the CTA can exit
+            for (int i = next - kNX; i < next; i += P)
                 if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
         }
     } else if (warp == 1) {
@@ -362,25 +398,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // k step over rows 256.. (D columns 256..), with the same A
         const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)(kTall ? 256 : TM));
         const uint32_t idesc2 = idesc_f16_f32(kTileN, (uint32_t)(kTall ? TM - 256 : 16));
+        int asl = 0;  // A slot s % na and its phase, advanced per slot (no runtime division)
+        uint32_t aph = 0;
         for (int s = 0; s < KS; ++s) {
-            const int xsl = s % kNX, asl = s % kNA;
+            const int xsl = s % kNX;
             if (!__all_sync(0xffffffffu, mbar_wait(&x_full[xsl], (s / kNX) & 1, abort_flag, err))) break;
-            if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], (s / kNA) & 1, abort_flag, err))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], aph, abort_flag, err))) break;
             tc_fence_after();
             if (elect_one()) {
-                const uint64_t bdesc = smem_desc_k128(xring + xsl * Cfg.x_stage);
 #pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk) {
-                    mma_f16_ts(d_tmem, a_tmem + asl * 32 + kk * 8, bdesc + 2 * kk, idesc,
-                               (s | kk) != 0);
-                    if (kTall)  // rows 256.. start 256 x 128 bytes into the stage
-                        mma_f16_ts(d_tmem + 256, a_tmem + asl * 32 + kk * 8, bdesc + (256 * 128 >> 4) + 2 * kk,
-                                   idesc2, (s | kk) != 0);
+                for (int kk = 0; kk < kSK / 16; ++kk) {
+                    // chunk kk / 4 of the stage; a K = 16 step is 32 bytes along its rows
+                    const uint64_t bdesc =
+                        smem_desc_k128(xring + xsl * Cfg.x_stage + (kk >> 2) * TM * 128) + 2 * (kk & 3);
+                    const uint32_t acol = a_tmem + asl * kSlotCols + kk * 8;
+                    mma_f16_ts(d_tmem, acol, bdesc, idesc, (s | kk) != 0);
+                    if (kTall)  // rows 256.. start 256 x 128 bytes into the chunk
+                        mma_f16_ts(d_tmem + 256, acol, bdesc + (256 * 128 >> 4), idesc2, (s | kk) != 0);
                 }
                 mma_commit(&x_empty[xsl]);
                 mma_commit(&a_empty[asl]);
             }
             __syncwarp();
+            if (++asl == na) {
+                asl = 0;
+                aph ^= 1;
+            }
         }
         if (elect_one()) mma_commit(d_full);
         __syncwarp();
@@ -400,6 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             sv[t] = i < TM && m0 + i < M ? __ldg(xscale + m0 + i) : 0.f;
         }
         bool ok = true;
+        int asl = 0;  // A slot and its phase, advanced per slot
+        uint32_t aph = 0;
         for (int ws = 0; ws < KWS && ok; ++ws) {
             const int wsl = ws % kNW;
             ok = __all_sync(0xffffffffu, mbar_wait(&w_full[wsl], (ws / kNW) & 1, abort_flag, err));
@@ -408,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stride the eight lanes of each load phase hit distinct 16-byte
             // bank groups (4-byte loads would conflict four ways).  The stage
             // goes back to the producer once every lane has used its row (after
-            // the last sub-slot): the next TMA fill of the slot is an
-            // async-proxy write and must not overtake shared loads in flight.
+            // the last slot): the next TMA fill of the slot is an async-proxy
+            // write and must not overtake shared loads in flight.
             const uint4 *row = reinterpret_cast<const uint4 *>(wring + wsl * kWStageBytes + r * kWRowBytes);
             uint32_t rw[36];
 #pragma unroll
@@ -424,37 +469,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage: a branch per block cost about a tenth of the rate
             bool large = true;
 #pragma unroll
-            for (int sub = 0; sub < kKW / kKB; ++sub)
-                large = large && scale_is_large(rw[9 * sub] & 0xFFFFu) && scale_is_large(rw[9 * sub + 4] >> 16);
-            auto stage_subs = [&](auto any_c) {
+            for (int q = 0; q < kKW / 64; ++q)
+                large = large && scale_is_large(rw[9 * q] & 0xFFFFu) && scale_is_large(rw[9 * q + 4] >> 16);
+            auto stage_slots = [&](auto any_c) {
                 constexpr bool kAny = decltype(any_c)::value;
 #pragma unroll
-                for (int sub = 0; sub < kKW / kKB; ++sub) {
-                    const int s = ws * (kKW / kKB) + sub, asl = s % kNA;
-                    ok = __all_sync(0xffffffffu,
-                                    mbar_wait(&a_empty[asl], ((s / kNA) & 1) ^ 1, abort_flag, err));
+                for (int sub = 0; sub < kSlotsPerW; ++sub) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[asl], aph ^ 1, abort_flag, err));
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t *wv = rw + 9 * sub;
-                    const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16),
-                                            __funnelshift_r(wv[1], wv[2], 16),
-                                            __funnelshift_r(wv[2], wv[3], 16),
-                                            __funnelshift_r(wv[3], wv[4], 16)};
-                    const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
-                    uint32_t cols[32];
-                    dequant_block<kAny>(wv[0] & 0xFFFFu, Q0, cols);
-                    dequant_block<kAny>(wv[4] >> 16, Q1, cols + 16);
-                    tmem_st32(a_tmem + lane_base + asl * 32, cols);
+                    // the slot's 64-k pieces: two blocks, 32 TMEM columns each
+#pragma unroll
+                    for (int pc = 0; pc < kChunks; ++pc) {
+                        const uint32_t *wv = rw + 9 * (sub * kChunks + pc);
+                        const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16),
+                                                __funnelshift_r(wv[1], wv[2], 16),
+                                                __funnelshift_r(wv[2], wv[3], 16),
+                                                __funnelshift_r(wv[3], wv[4], 16)};
+                        const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+                        uint32_t cols[32];
+                        dequant_block<kAny>(wv[0] & 0xFFFFu, Q0, cols);
+                        dequant_block<kAny>(wv[4] >> 16, Q1, cols + 16);
+                        tmem_st32(a_tmem + lane_base + asl * kSlotCols + pc * 32, cols);
+                    }
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();  // every lane's stores are done
                     if (lane == 0) mbar_arrive(&a_full[asl]);
+                    if (++asl == na) {
+                        asl = 0;
+                        aph ^= 1;
+                    }
                 }
             };
             if (__all_sync(0xffffffffu, large))
-                stage_subs(std::integral_constant<bool, false>{});
+                stage_slots(std::integral_constant<bool, false>{});
             else
-                stage_subs(std::integral_constant<bool, true>{});
+                stage_slots(std::integral_constant<bool, true>{});
             if (lane == 0) mbar_arrive(&w_empty[wsl]);
         }
         // epilogue: D[row r][column m] -> y[m][n0 + r], times the x row's
@@ -547,7 +598,7 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
     {
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {kKB, (cuuint32_t)(TM <= 256 ? TM : TM / 2)};
+        const cuuint32_t box[2] = {64, (cuuint32_t)(TM <= 256 ? TM : TM / 2)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x16), dims, strides, box,
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -565,9 +616,17 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const bool tall = TM > 256;
-    auto kernel = tall ? gemm_kernel<true, kNXTall>
-                       : (nx == kNXPair ? gemm_kernel<false, kNXPair> : gemm_kernel<false, kNXShort>);
+    // the instantiation for the tile's slot size and x ring (kNXMid and
+    // kNXPair have the same depth: the slot size tells them apart)
+    using Kernel = decltype(&gemm_kernel<false, kNXShort, 64>);
+    Kernel kernel = nullptr;
+    if (slot_k(TM) == 128)
+        kernel = TM > 256 && nx == kNXTall ? gemm_kernel<true, kNXTall, 128>
+                 : nx == kNXMid            ? gemm_kernel<false, kNXMid, 128>
+                                           : nullptr;
+    else
+        kernel = nx == kNXPair ? gemm_kernel<false, kNXPair, 64> : nx == kNXShort ? gemm_kernel<false, kNXShort, 64> : nullptr;
+    if (!kernel || (TM > 256) != (kernel == gemm_kernel<true, kNXTall, 128>)) return cudaErrorInvalidConfiguration;
     e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(((N + kTileN - 1) / kTileN) * ((M + TM - 1) / TM)), 1, (unsigned)splits);
