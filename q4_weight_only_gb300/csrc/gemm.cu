@@ -82,7 +82,12 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
 }
 
 // k per A slot and x stage for a tile of tm rows.
-__host__ __device__ constexpr int slot_k(int tm) {
+__host__ __device__ constexpr int slot_k(int tm) { return tm >= kWideSlotMinRows ? 128 : 64; }
+// k per x stage: 128 where the ring holds two or three such stages (tall
+// tiles, 129..192 rows); tiles of 193..256 rows take their x in five 64-k
+// chunks, two per A slot, so that the ring keeps as much x in flight as
+// with 64-k slots
+__host__ __device__ constexpr int xstage_k(int tm) {
     return tm > kMaxTileRowsShort || (tm >= kWideSlotMinRows && tm <= kWideSlotMaxRows) ? 128 : 64;
 }
 
@@ -96,7 +101,7 @@ struct GemmLayout {
     int num_bars, na;
     __host__ __device__ GemmLayout(int tm, int nx) {
         const int sk = slot_k(tm);
-        x_stage = (uint32_t)tm * 2 * sk;
+        x_stage = (uint32_t)tm * 2 * xstage_k(tm);
         d_cols = tm < 32 ? 32 : (uint32_t)((tm + 31) / 32 * 32);
         const int budget = d_cols <= 128 ? 256 : 512;
         na = (budget - (int)d_cols) / (sk / 2) < kNAMax ? (budget - (int)d_cols) / (sk / 2) : kNAMax;
@@ -114,7 +119,7 @@ struct GemmLayout {
 // than SMs to pair up; a CTA alone on its SM keeps the deep ring.
 int x_ring_stages(int tm, int64_t ctas, int sms) {
     if (tm > kMaxTileRowsShort) return kNXTall;
-    if (tm > kWideSlotMaxRows) return kNXShort;
+    if (tm > kWideSlotMaxRows) return kNXShort;  // five 64-k chunks
     if (tm >= kWideSlotMinRows) return kNXMid;
     if (tm > 80 && tm <= kPairMaxRows && ctas > sms) return kNXPair;
     return kNXShort;
@@ -273,12 +278,14 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
 // kTall: x tiles of more than 256 rows (two TMA boxes per x chunk, a second
 // MMA per k step); a separate instantiation keeps the common path unchanged.
 // kNX: stages of the x ring.  kSK: k per A slot and x stage (slot_k(TM)).
-template <bool kTall, int kNX, int kSK>
+template <bool kTall, int kNX, int kSK, int kXK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 float *__restrict__ y, float *__restrict__ part, const float *__restrict__ xscale, int M, int N,
                 int K, int TM, int ybf16, unsigned int *err) {
-    constexpr int kChunks = kSK / 64;         // 64-k pieces per slot (x TMA boxes, A stores)
+    constexpr int kChunks = kSK / 64;         // 64-k pieces per slot (A stores)
+    constexpr int kXPerSlot = kSK / kXK;      // x stages per A slot
+    constexpr int kXChunks = kXK / 64;        // 64-k chunks (TMA boxes) per x stage
     constexpr int kSlotsPerW = kKW / kSK;     // A slots per weight stage
     constexpr int kSlotCols = kSK / 2;        // TMEM columns per A slot
     const GemmLayout Cfg(TM, kNX);
@@ -372,15 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int P = kNX % 2 == 0 ? 2 : 1;
         const int p = warp - kXProducerWarp;
         if (lane == 0 && p < P) {
+            const int KX = KS * kXPerSlot;  // x stages of this CTA's K range
             int next = p;  // first stage not issued
-            for (int s = p; s < KS; s += P) {
+            for (int s = p; s < KX; s += P) {
                 const int xsl = s % kNX;
                 if (!mbar_wait(&x_empty[xsl], ((s / kNX) & 1) ^ 1, abort_flag, err)) break;
                 mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
                 uint8_t *dst = xring + xsl * Cfg.x_stage;
 #pragma unroll
-                for (int j = 0; j < kChunks; ++j) {
-                    const int kx = w_begin * kKW + s * kSK + 64 * j;
+                for (int j = 0; j < kXChunks; ++j) {
+                    const int kx = w_begin * kKW + s * kXK + 64 * j;
                     tma_load_2d(dst + j * TM * 128, &xmap, kx, m0, &x_full[xsl]);
                     if (kTall)  // a TMA box is at most 256 rows: two boxes of TM / 2
                         tma_load_2d(dst + j * TM * 128 + (TM / 2) * 128, &xmap, kx, m0 + TM / 2, &x_full[xsl]);
@@ -400,23 +408,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc2 = idesc_f16_f32(kTileN, (uint32_t)(kTall ? TM - 256 : 16));
         int asl = 0;  // A slot s % na and its phase, advanced per slot (no runtime division)
         uint32_t aph = 0;
-        for (int s = 0; s < KS; ++s) {
-            const int xsl = s % kNX;
-            if (!__all_sync(0xffffffffu, mbar_wait(&x_full[xsl], (s / kNX) & 1, abort_flag, err))) break;
+        bool ok = true;
+        for (int s = 0; ok && s < KS; ++s) {
+            // the slot's x stages g = s * kXPerSlot + u
+#pragma unroll
+            for (int u = 0; u < kXPerSlot; ++u) {
+                const int g = s * kXPerSlot + u;
+                ok = __all_sync(0xffffffffu, mbar_wait(&x_full[g % kNX], (g / kNX) & 1, abort_flag, err));
+                if (!ok) break;
+            }
+            if (!ok) break;
             if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], aph, abort_flag, err))) break;
             tc_fence_after();
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kSK / 16; ++kk) {
-                    // chunk kk / 4 of the stage; a K = 16 step is 32 bytes along its rows
+                    // 64-k chunk kk / 4 of the slot: x stage u, chunk jj of it;
+                    // a K = 16 step is 32 bytes along its rows
+                    const int chunk = kk >> 2, u = chunk / kXChunks, jj = chunk % kXChunks;
+                    const int g = s * kXPerSlot + u;
                     const uint64_t bdesc =
-                        smem_desc_k128(xring + xsl * Cfg.x_stage + (kk >> 2) * TM * 128) + 2 * (kk & 3);
+                        smem_desc_k128(xring + (g % kNX) * Cfg.x_stage + jj * TM * 128) + 2 * (kk & 3);
                     const uint32_t acol = a_tmem + asl * kSlotCols + kk * 8;
                     mma_f16_ts(d_tmem, acol, bdesc, idesc, (s | kk) != 0);
                     if (kTall)  // rows 256.. start 256 x 128 bytes into the chunk
                         mma_f16_ts(d_tmem + 256, acol, bdesc + (256 * 128 >> 4), idesc2, (s | kk) != 0);
                 }
-                mma_commit(&x_empty[xsl]);
+#pragma unroll
+                for (int u = 0; u < kXPerSlot; ++u) mma_commit(&x_empty[(s * kXPerSlot + u) % kNX]);
                 mma_commit(&a_empty[asl]);
             }
             __syncwarp();
@@ -618,15 +637,19 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
     }
     // the instantiation for the tile's slot size and x ring (kNXMid and
     // kNXPair have the same depth: the slot size tells them apart)
-    using Kernel = decltype(&gemm_kernel<false, kNXShort, 64>);
+    using Kernel = decltype(&gemm_kernel<false, kNXShort, 64, 64>);
     Kernel kernel = nullptr;
-    if (slot_k(TM) == 128)
-        kernel = TM > 256 && nx == kNXTall ? gemm_kernel<true, kNXTall, 128>
-                 : nx == kNXMid            ? gemm_kernel<false, kNXMid, 128>
+    if (slot_k(TM) == 128 && xstage_k(TM) == 128)
+        kernel = TM > 256 && nx == kNXTall ? gemm_kernel<true, kNXTall, 128, 128>
+                 : nx == kNXMid            ? gemm_kernel<false, kNXMid, 128, 128>
                                            : nullptr;
+    else if (slot_k(TM) == 128)
+        kernel = TM <= 256 && nx == kNXShort ? gemm_kernel<false, kNXShort, 128, 64> : nullptr;
     else
-        kernel = nx == kNXPair ? gemm_kernel<false, kNXPair, 64> : nx == kNXShort ? gemm_kernel<false, kNXShort, 64> : nullptr;
-    if (!kernel || (TM > 256) != (kernel == gemm_kernel<true, kNXTall, 128>)) return cudaErrorInvalidConfiguration;
+        kernel = nx == kNXPair    ? gemm_kernel<false, kNXPair, 64, 64>
+                 : nx == kNXShort ? gemm_kernel<false, kNXShort, 64, 64>
+                                  : nullptr;
+    if (!kernel || (TM > 256) != (kernel == gemm_kernel<true, kNXTall, 128, 128>)) return cudaErrorInvalidConfiguration;
     e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(((N + kTileN - 1) / kTileN) * ((M + TM - 1) / TM)), 1, (unsigned)splits);
