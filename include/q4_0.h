@@ -290,6 +290,21 @@ int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y,
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * q4_0_gemm_plan -- the launch q4_0_gemm makes for (M, N, K) with its
+ * default workspace (q4_0_gemm_workspace_bytes) on the current device, and
+ * that q4_0_matmul makes for M > 64.  No work is launched.
+ *   *tile_rows  : x rows per output tile (a multiple of 16, at most 320)
+ *   *splits     : ways K is split over CTAs (1..4; partial tiles summed in
+ *                 split order afterwards)
+ *   *persistent : 1 when one CTA per SM takes several tiles in turn (tiles of
+ *                 193..256 rows, at least two tiles per SM, no split), else
+ *                 0 (one CTA per tile)
+ * Errors: Q4_0_ERR_INVALID_ARG for a null output pointer, M, N < 1 or
+ * K % 256 != 0; Q4_0_ERR_CUDA when no device is current.
+ */
+int q4_0_gemm_plan(int64_t M, int64_t N, int64_t K, int *tile_rows, int *splits, int *persistent);
+
+/*
  * q4_0_gemm_noalloc -- q4_0_gemm for callers that cannot allocate device
  * memory and have no workspace to hand over.  The paper has no counterpart:
  * this entry point exists for callers where the CUDA allocator must not be

@@ -47,6 +47,7 @@ SIGNATURES = {
     "q4_0_gemm_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "q4_0_gemm": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _INT),
     "q4_0_gemm_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "q4_0_gemm_plan": ([_I64, _I64, _I64, _P, _P, _P], _INT),
     "q4_0_selftest_wait_timeout": ([_I64, _P], _INT),
     "q4_0_device_error": ([ctypes.POINTER(_INT)], _INT),
 }
@@ -310,6 +311,14 @@ def gemm(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = 
                            ws.data_ptr(), wsb, _stream(stream)), "q4_0_gemm")
     return out
 
+
+
+def gemm_plan(M: int, N: int, K: int) -> dict:
+    """The launch q4_0_gemm makes for (M, N, K) on the current device:
+    {"tile_rows", "splits", "persistent"} (include/q4_0.h, q4_0_gemm_plan)."""
+    tr, sp, pe = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().q4_0_gemm_plan(M, N, K, ctypes.byref(tr), ctypes.byref(sp), ctypes.byref(pe)), "q4_0_gemm_plan")
+    return {"tile_rows": tr.value, "splits": sp.value, "persistent": bool(pe.value)}
 
 def gemm_noalloc(x: torch.Tensor, wq: torch.Tensor, N: int, K: int, out: torch.Tensor = None,
                  stream=None) -> torch.Tensor:

@@ -174,6 +174,17 @@ size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return gemm_workspace_bytes(M, N, K, current_splits(M, N, K));
 }
 
+int q4_0_gemm_plan(int64_t M, int64_t N, int64_t K, int *tile_rows, int *splits, int *persistent) {
+    if (!tile_rows || !splits || !persistent || M < 1 || N < 1 || K < 256 || K % 256 != 0)
+        return Q4_0_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4_0_ERR_CUDA;
+    const int sms = device_sm_count(dev);
+    *splits = gemm_splits(M, N, K, sms);
+    gemm_plan(M, N, K, sms, *splits, tile_rows, persistent);
+    return Q4_0_OK;
+}
+
 size_t q4_0_gemv_workspace_bytes(int64_t M, int64_t K) {
     if (M < 1 || M > kGemvMaxM || K < 1) return 0;
     return gemv_workspace_bytes(M, K);

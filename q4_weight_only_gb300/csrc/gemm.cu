@@ -107,11 +107,21 @@ struct GemmLayout {
         na = (budget - (int)d_cols) / (sk / 2) < kNAMax ? (budget - (int)d_cols) / (sk / 2) : kNAMax;
         cols = pow2_at_least(d_cols + na * (sk / 2));
         bar_off = (size_t)nx * x_stage + (size_t)kNW * kWStageBytes;
-        num_bars = 2 * kNW + 2 * nx + 2 * kNAMax + 2;
-        scale_off = bar_off + num_bars * 8 + 16;  // the tile's x-row scales (tm rounded up to 32 floats)
-        smem = 1024 + scale_off + (size_t)((tm + 31) / 32 * 32) * 4;
+        num_bars = 2 * kNW + 2 * nx + 2 * kNAMax + 3;
+        // the tile's x-row scales (tm rounded up to 32 floats), read as float4:
+        // 16-byte aligned whatever the barrier count
+        scale_off = (bar_off + num_bars * 8 + 16 + 15) / 16 * 16;
+        smem = 1024 + scale_off + 2 * (size_t)((tm + 31) / 32 * 32) * 4;  // two scale buffers (persistent form)
     }
 };
+
+// The persistent form runs tiles of 193..256 rows (one MMA wide, 128-k slots
+// fed by 64-k x chunks) when there are at least two tiles per SM and no K
+// split.
+bool use_persistent(int tm, int nx, int64_t tiles, int splits, int sms) {
+    return splits == 1 && tm > kWideSlotMaxRows && tm <= kMaxTileRowsShort && nx == kNXShort &&
+           slot_k(tm) == 128 && xstage_k(tm) == 64 && sms > 0 && tiles >= 2 * (int64_t)sms;
+}
 
 // x ring depth for a tile of tm rows when the launch has `ctas` CTAs on
 // `sms` SMs: the shallow ring where it lets a second CTA share the SM
@@ -275,6 +285,20 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
     }
 }
 
+// Tile b of the launch order -> its first weight row n0 and x row m0.  Tiles
+// come in bands of up to kBandMTiles x tiles; within a band, the x tiles of
+// one weight tile are neighbours, so a weight tile comes from HBM once per
+// band while the band's x rows stay in L2.
+__device__ __forceinline__ void tile_origin(int64_t b, int NT, int MT, int TM, int &n0, int &m0) {
+    const int64_t per_band = (int64_t)NT * kBandMTiles;
+    const int bands = (MT + kBandMTiles - 1) / kBandMTiles;
+    const int band = (int)(b / per_band < bands - 1 ? b / per_band : bands - 1);
+    const int64_t r = b - (int64_t)band * per_band;
+    const int gm = MT - band * kBandMTiles < kBandMTiles ? MT - band * kBandMTiles : kBandMTiles;
+    n0 = (int)(r / gm) * kTileN;
+    m0 = (band * kBandMTiles + (int)(r % gm)) * TM;
+}
+
 // kTall: x tiles of more than 256 rows (two TMA boxes per x chunk, a second
 // MMA per k step); a separate instantiation keeps the common path unchanged.
 // kNX: stages of the x ring.  kSK: k per A slot and x stage (slot_k(TM)).
@@ -305,21 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *xs_tile = reinterpret_cast<float *>(smem + Cfg.scale_off);  // [TM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // tile order: bands of up to kBandMTiles x tiles; within a band, the x
-    // tiles of one weight tile are neighbours, so a weight tile comes from
-    // HBM once per band while the band's x rows stay in L2
     const int NT = (N + kTileN - 1) / kTileN, MT = (M + TM - 1) / TM;
     int n0, m0;
-    {
-        const int64_t b = blockIdx.x;
-        const int64_t per_band = (int64_t)NT * kBandMTiles;
-        const int bands = (MT + kBandMTiles - 1) / kBandMTiles;
-        const int band = (int)(b / per_band < bands - 1 ? b / per_band : bands - 1);
-        const int64_t r = b - (int64_t)band * per_band;
-        const int gm = MT - band * kBandMTiles < kBandMTiles ? MT - band * kBandMTiles : kBandMTiles;
-        n0 = (int)(r / gm) * kTileN;
-        m0 = (band * kBandMTiles + (int)(r % gm)) * TM;
-    }
+    tile_origin(blockIdx.x, NT, MT, TM, n0, m0);
     // split-K: CTA z of gridDim.z takes weight stages [w_begin, w_end) and,
     // when split, writes its partial tile to part[z] instead of y
     const int KW_all = K / kKW;
@@ -582,6 +594,304 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Persistent form of gemm_kernel for tiles of one MMA width fed by 64-k x
+// chunks, when there are at least two tiles per SM and no K split: one CTA
+// per SM takes tiles u = c, c + G, ... of the band order.  Four extra warps
+// run the epilogue, so that while they store tile i the producers and the
+// dequantising warps already work on tile i + 1 (its copies land and its
+// first A slots fill); the MMAs of tile i + 1 start once the epilogue has
+// read the accumulator.  One-tile-per-CTA launches paid the CTA's start,
+// its pipeline fill and the gap to the next CTA on every tile.
+// Warps: 0 weight copies, 1 MMA issue, 2-5 dequantisation, 6 x copies
+// (7 idle), 8-11 epilogue.
+constexpr int kPThreads = 384;
+constexpr int kPEpiWarp0 = 8;
+
+template <int kNX, int kSK, int kXK>
+__global__ void __launch_bounds__(kPThreads, 1)
+    gemm_persistent_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                           float *__restrict__ y, const float *__restrict__ xscale, int M, int N, int K, int TM,
+                           int ybf16, unsigned int *err) {
+    constexpr int kChunks = kSK / 64;
+    constexpr int kXPerSlot = kSK / kXK;
+    constexpr int kXChunks = kXK / 64;
+    constexpr int kSlotsPerW = kKW / kSK;
+    constexpr int kSlotCols = kSK / 2;
+    constexpr int P = kNX % 2 == 0 ? 2 : 1;  // x producers (warps 6 and 7 for an even ring)
+    const GemmLayout Cfg(TM, kNX);
+    const int na = Cfg.na;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *xring = smem;
+    uint8_t *wring = smem + kNX * Cfg.x_stage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg.bar_off);
+    uint64_t *w_full = bars, *w_empty = bars + kNW;
+    uint64_t *x_full = bars + 2 * kNW, *x_empty = x_full + kNX;
+    uint64_t *a_full = x_empty + kNX, *a_empty = a_full + kNAMax;
+    uint64_t *d_full = a_empty + kNAMax, *d_empty = d_full + 1, *drain = d_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg.num_bars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int scale_rows = (TM + 31) / 32 * 32;
+    float *xs2 = reinterpret_cast<float *>(smem + Cfg.scale_off);  // [2][scale_rows]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NT = (N + kTileN - 1) / kTileN, MT = (M + TM - 1) / TM;
+    const int64_t units = (int64_t)NT * MT;
+    const int my_tiles = units > (int64_t)blockIdx.x ? (int)((units - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    const int KW = K / kKW, KS = KW * kSlotsPerW, KX = KS * kXPerSlot;
+    auto origin = [&](int i, int &n0, int &m0) {
+        tile_origin((int64_t)blockIdx.x + (int64_t)i * gridDim.x, NT, MT, TM, n0, m0);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNW; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&w_empty[i], 4);  // one arrival per dequant warp
+        }
+        for (int i = 0; i < kNX; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);
+        }
+        for (int i = 0; i < na; ++i) {
+            mbar_init(&a_full[i], 4);
+            mbar_init(&a_empty[i], 1);
+        }
+        mbar_init(d_full, 1);
+        mbar_init(d_empty, 4);  // one arrival per epilogue warp
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&wmap);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, Cfg.cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_launch_dependents();
+    pdl_wait();  // x16 comes from the previous kernel
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t d_tmem = tmem;
+    const uint32_t a_tmem = tmem + Cfg.d_cols;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // the weight stages of every tile, in order (g counts them)
+            int g = 0;
+            bool ok = true;
+            for (int i = 0; ok && i < my_tiles; ++i) {
+                int n0, m0;
+                origin(i, n0, m0);
+                for (int ws = 0; ws < KW; ++ws, ++g) {
+                    const int wsl = g % kNW;
+                    if (!mbar_wait(&w_empty[wsl], ((g / kNW) & 1) ^ 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&w_full[wsl], kWStageBytes);
+                    tma_load_2d(wring + wsl * kWStageBytes, &wmap, ws * kWRowBytes, n0, &w_full[wsl]);
+                }
+            }
+            // let every issued copy land before the CTA can exit
+            for (int i = g - kNW; i < g; ++i)
+                if (i >= 0) mbar_drain(&w_full[i % kNW], (i / kNW) & 1);
+        }
+    } else if (warp == kXProducerWarp || warp == kXProducerWarp + 1) {
+        // the x stages of every tile: producer p takes stages p, p + P, ...
+        const int p = warp - kXProducerWarp;
+        if (lane == 0 && p < P) {
+            int next = p;  // first stage (counted over all tiles) not issued
+            bool ok = true;
+            for (int i = 0; ok && i < my_tiles; ++i) {
+                int n0, m0;
+                origin(i, n0, m0);
+                for (int s = 0; s < KX; ++s) {
+                    const int g = i * KX + s;
+                    if (g % P != p) continue;
+                    const int xsl = g % kNX;
+                    if (!mbar_wait(&x_empty[xsl], ((g / kNX) & 1) ^ 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
+#pragma unroll
+                    for (int j = 0; j < kXChunks; ++j)
+                        tma_load_2d(xring + xsl * Cfg.x_stage + j * TM * 128, &xmap, s * kXK + 64 * j, m0,
+                                    &x_full[xsl]);
+                    next = g + P;
+                }
+            }
+            for (int i = next - kNX; i < next; i += P)
+                if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
+        }
+    } else if (warp == 1) {
+        // MMA issue; tile i waits until the epilogue has read tile i - 1
+        const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)TM);
+        int asl = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int i = 0; ok && i < my_tiles; ++i) {
+            if (!__all_sync(0xffffffffu, mbar_wait(d_empty, (i & 1) ^ 1, abort_flag, err))) break;
+            tc_fence_after();
+            for (int s = 0; s < KS; ++s) {
+#pragma unroll
+                for (int u = 0; u < kXPerSlot; ++u) {
+                    const int g = (i * KS + s) * kXPerSlot + u;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&x_full[g % kNX], (g / kNX) & 1, abort_flag, err));
+                    if (!ok) break;
+                }
+                if (!ok) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&a_full[asl], aph, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < kSK / 16; ++kk) {
+                        const int chunk = kk >> 2, u = chunk / kXChunks, jj = chunk % kXChunks;
+                        const int g = (i * KS + s) * kXPerSlot + u;
+                        const uint64_t bdesc =
+                            smem_desc_k128(xring + (g % kNX) * Cfg.x_stage + jj * TM * 128) + 2 * (kk & 3);
+                        mma_f16_ts(d_tmem, a_tmem + asl * kSlotCols + kk * 8, bdesc, idesc, (s | kk) != 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kXPerSlot; ++u) mma_commit(&x_empty[((i * KS + s) * kXPerSlot + u) % kNX]);
+                    mma_commit(&a_empty[asl]);
+                }
+                __syncwarp();
+                if (++asl == na) {
+                    asl = 0;
+                    aph ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (elect_one()) mma_commit(d_full);
+            __syncwarp();
+        }
+    } else if (warp >= 2 && warp < kXProducerWarp) {
+        // warps 2..5: dequantise every tile's weight stages into the A slots
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        int g = 0, asl = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int i = 0; ok && i < my_tiles; ++i) {
+            for (int ws = 0; ws < KW && ok; ++ws, ++g) {
+                const int wsl = g % kNW;
+                ok = __all_sync(0xffffffffu, mbar_wait(&w_full[wsl], (g / kNW) & 1, abort_flag, err));
+                if (!ok) break;
+                const uint4 *row = reinterpret_cast<const uint4 *>(wring + wsl * kWStageBytes + r * kWRowBytes);
+                uint32_t rw[36];
+#pragma unroll
+                for (int q = 0; q < 9; ++q) {
+                    const uint4 v = row[q];
+                    rw[4 * q + 0] = v.x;
+                    rw[4 * q + 1] = v.y;
+                    rw[4 * q + 2] = v.z;
+                    rw[4 * q + 3] = v.w;
+                }
+                bool large = true;
+#pragma unroll
+                for (int q = 0; q < kKW / 64; ++q)
+                    large = large && scale_is_large(rw[9 * q] & 0xFFFFu) && scale_is_large(rw[9 * q + 4] >> 16);
+                auto stage_slots = [&](auto any_c) {
+                    constexpr bool kAny = decltype(any_c)::value;
+#pragma unroll
+                    for (int sub = 0; sub < kSlotsPerW; ++sub) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[asl], aph ^ 1, abort_flag, err));
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int pc = 0; pc < kChunks; ++pc) {
+                            const uint32_t *wv = rw + 9 * (sub * kChunks + pc);
+                            const uint32_t Q0[4] = {__funnelshift_r(wv[0], wv[1], 16),
+                                                    __funnelshift_r(wv[1], wv[2], 16),
+                                                    __funnelshift_r(wv[2], wv[3], 16),
+                                                    __funnelshift_r(wv[3], wv[4], 16)};
+                            const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
+                            uint32_t cols[32];
+                            dequant_block<kAny>(wv[0] & 0xFFFFu, Q0, cols);
+                            dequant_block<kAny>(wv[4] >> 16, Q1, cols + 16);
+                            tmem_st32(a_tmem + lane_base + asl * kSlotCols + pc * 32, cols);
+                        }
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&a_full[asl]);
+                        if (++asl == na) {
+                            asl = 0;
+                            aph ^= 1;
+                        }
+                    }
+                };
+                if (__all_sync(0xffffffffu, large))
+                    stage_slots(std::integral_constant<bool, false>{});
+                else
+                    stage_slots(std::integral_constant<bool, true>{});
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(&w_empty[wsl]);
+            }
+        }
+    } else if (warp >= kPEpiWarp0) {
+        // warps 8..11: epilogue.  D[row r][column m] -> y[m][n0 + r], times
+        // the x row's 2^-shift; the accumulator goes back to the MMA warp
+        // once every lane's loads are done
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const int et = threadIdx.x - kPEpiWarp0 * 32;  // 0..127
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        for (int i = 0; i < my_tiles; ++i) {
+            int n0, m0;
+            origin(i, n0, m0);
+            // the tile's x-row scales (buffer i % 2: the other warps may
+            // still read the previous tile's)
+            float *xs = xs2 + (i & 1) * scale_rows;
+            for (int j = et; j < scale_rows; j += 128) xs[j] = j < TM && m0 + j < M ? __ldg(xscale + m0 + j) : 0.f;
+            named_bar_sync(2, 128);  // the four epilogue warps
+            if (!__all_sync(0xffffffffu, mbar_wait(d_full, i & 1, abort_flag, err))) break;
+            tc_fence_after();
+            const int n = n0 + r;
+            for (int c = 0; c < TM; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(d_tmem + lane_base + c, v);
+                float sc[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 t = reinterpret_cast<const float4 *>(xs + c)[q];
+                    sc[4 * q] = t.x;
+                    sc[4 * q + 1] = t.y;
+                    sc[4 * q + 2] = t.z;
+                    sc[4 * q + 3] = t.w;
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int m = m0 + c + j;
+                    if (c + j < TM && m < M && n < N)
+                        store_y(y, (int64_t)m * N + n, __uint_as_float(v[j]) * sc[j], ybf16 != 0);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(d_empty);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        if (lane == 0) {
+            // every MMA issued by this CTA has finished before TMEM is released
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg.cols);
+    }
+}
+
 // ----------------------------------------------------------------- host
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -650,9 +960,19 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
                  : nx == kNXShort ? gemm_kernel<false, kNXShort, 64, 64>
                                   : nullptr;
     if (!kernel || (TM > 256) != (kernel == gemm_kernel<true, kNXTall, 128, 128>)) return cudaErrorInvalidConfiguration;
+    const int64_t tiles = ((N + kTileN - 1) / kTileN) * ((M + TM - 1) / TM);
+    const int sms = device_sm_count(dev);
+    if (use_persistent(TM, nx, tiles, splits, sms)) {
+        // many 256-row tiles: the persistent form (one CTA per SM)
+        auto pk = gemm_persistent_kernel<kNXShort, 128, 64>;
+        e = ensure_smem_attr(reinterpret_cast<const void *>(pk), (int)Cfg.smem);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(pk, dim3((unsigned)sms), dim3(kPThreads), Cfg.smem, s, xmap, wmap, y, xscale, (int)M,
+                          (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
+    }
     e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)(((N + kTileN - 1) / kTileN) * ((M + TM - 1) / TM)), 1, (unsigned)splits);
+    const dim3 grid((unsigned)tiles, 1, (unsigned)splits);
     e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr, xscale,
                    (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
     if (e != cudaSuccess || splits == 1) return e;
@@ -711,6 +1031,14 @@ bool gemm_shape_supported(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 1) return false;
     const int tm = tile_rows(M);
     return ((N + kTileN - 1) / kTileN) * ((M + tm - 1) / tm) <= 0x7FFFFFFF && M <= 0x7FFFFFFF;
+}
+
+void gemm_plan(int64_t M, int64_t N, int64_t K, int sms, int splits, int *tile_rows_out, int *persistent_out) {
+    const int tm = tile_rows(M);
+    const int64_t tiles = ((N + kTileN - 1) / kTileN) * ((M + tm - 1) / tm);
+    const int nx = x_ring_stages(tm, tiles * splits, sms);
+    *tile_rows_out = tm;
+    *persistent_out = use_persistent(tm, nx, tiles, splits, sms) ? 1 : 0;
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {

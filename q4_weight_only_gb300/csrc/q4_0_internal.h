@@ -97,6 +97,9 @@ cudaError_t launch_pad(const uint16_t *x, const uint8_t *wq, int64_t M, int64_t 
 // split (splits > 1), the fp32 partial tiles: gemm_workspace_bytes(M, N, K,
 // splits) bytes.  gemm_splits picks the split for a device with `sms` SMs.
 int gemm_splits(int64_t M, int64_t N, int64_t K, int sms);
+// The launch plan of a GEMM with `splits` K splits on `sms` SMs: its x tile
+// rows and whether the persistent form runs.
+void gemm_plan(int64_t M, int64_t N, int64_t K, int sms, int splits, int *tile_rows, int *persistent);
 bool gemm_shape_supported(int64_t M, int64_t N, int64_t K);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
 cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,

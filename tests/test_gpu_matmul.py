@@ -464,3 +464,40 @@ def test_gemm_whole_waves_and_a_ragged_wave(M, K):
     check_full(y, x, wq, N, K)
     assert torch.equal(q4.gemm(xd, wd, N, K), y)
     assert q4.device_error() == 0
+
+
+def test_gemm_plan():
+    """The launch plan the library reports for the prefill shapes: 256-row
+    tiles run persistent at M = 2048 (QKV, O, gate+up) and split at down;
+    M = 272 is one tall tile; small M runs one CTA per tile."""
+    q4 = lib()
+    p = q4.gemm_plan(2048, 7168, 5120)
+    assert p == {"tile_rows": 256, "splits": 1, "persistent": True}
+    p = q4.gemm_plan(2048, 5120, 17408)
+    assert p["tile_rows"] == 256 and p["splits"] > 1 and not p["persistent"]
+    p = q4.gemm_plan(272, 34816, 5120)
+    assert p == {"tile_rows": 272, "splits": 1, "persistent": False}
+    assert not q4.gemm_plan(96, 5120, 5120)["persistent"]
+    with pytest.raises(q4.Q4Error):
+        q4.gemm_plan(64, 128, 300)
+
+
+def test_persistent_gemm_every_output():
+    """The persistent GEMM (one CTA per SM taking tiles in turn, the
+    accumulator drained by separate epilogue warps while the next tile's
+    copies and dequantisation run): ragged M and N, two or three tiles per
+    CTA; every output against the oracle, bitwise repeatable, and equal to
+    the dispatcher's result."""
+    q4 = lib()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, N, K = 500, 128 * (sms + 1) + 72, 512
+    assert q4.gemm_plan(M, N, K)["persistent"]
+    x, wq = case(9700, M, N, K, outlier_blocks=0.05, act_outliers=0.01)
+    xd, wd = x_dev(x), wq_dev(wq)
+    y = q4.gemm(xd, wd, N, K)
+    check_full(y, x, wq, N, K)
+    assert torch.equal(q4.gemm(xd, wd, N, K), y)
+    assert torch.equal(q4.matmul(xd, wd, N, K), y)
+    y16 = q4.matmul(xd, wd, N, K, out_dtype=torch.bfloat16)
+    assert torch.equal(y16, y.to(torch.bfloat16))
+    assert q4.device_error() == 0

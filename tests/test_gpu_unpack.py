@@ -170,6 +170,23 @@ def test_one_hot_gemm(v):
     assert q4.device_error() == 0
 
 
+
+def test_one_hot_persistent_gemm():
+    """x = I (M = K = 512, two 256-row x tiles) against a matrix of enough
+    weight tiles that the persistent GEMM runs: every (n, k) equals
+    RN16(w) exactly."""
+    q4 = lib()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N, K = 128 * (sms + 1) + 72, 512
+    assert q4.gemm_plan(K, N, K)["persistent"]
+    wq = q4_matrix(15, N, K)
+    wd = wq_dev(wq)
+    E = expected(wq, N, K, rounded16=True)
+    X = one_hot_x(K, 1.0)
+    Y = run_rows(lambda xs: q4.gemm(xs, wd, N, K), X, [0], N, K, K)
+    assert_exact(Y, E, 1.0, [0], K, K, "persistent GEMM")
+    assert q4.device_error() == 0
+
 def test_scale_classes_present():
     """The test matrices hold every scale class the kernels distinguish."""
     o = oracle.get()
