@@ -116,11 +116,11 @@ struct GemmLayout {
 };
 
 // The persistent form runs tiles of 193..256 rows (one MMA wide, 128-k slots
-// fed by 64-k x chunks) when there are at least two tiles per SM and no K
-// split.
+// fed by 64-k x chunks) when there are at least two work units (tiles times
+// K splits) per SM.
 bool use_persistent(int tm, int nx, int64_t tiles, int splits, int sms) {
-    return splits == 1 && tm > kWideSlotMaxRows && tm <= kMaxTileRowsShort && nx == kNXShort &&
-           slot_k(tm) == 128 && xstage_k(tm) == 64 && sms > 0 && tiles >= 2 * (int64_t)sms;
+    return tm > kWideSlotMaxRows && tm <= kMaxTileRowsShort && nx == kNXShort && slot_k(tm) == 128 &&
+           xstage_k(tm) == 64 && sms > 0 && tiles * splits >= 2 * (int64_t)sms;
 }
 
 // x ring depth for a tile of tm rows when the launch has `ctas` CTAs on
@@ -610,8 +610,8 @@ constexpr int kPEpiWarp0 = 8;
 template <int kNX, int kSK, int kXK>
 __global__ void __launch_bounds__(kPThreads, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                           float *__restrict__ y, const float *__restrict__ xscale, int M, int N, int K, int TM,
-                           int ybf16, unsigned int *err) {
+                           float *__restrict__ y, float *__restrict__ part, const float *__restrict__ xscale, int M,
+                           int N, int K, int TM, int splits, int ybf16, unsigned int *err) {
     constexpr int kChunks = kSK / 64;
     constexpr int kXPerSlot = kSK / kXK;
     constexpr int kXChunks = kXK / 64;
@@ -637,11 +637,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NT = (N + kTileN - 1) / kTileN, MT = (M + TM - 1) / TM;
-    const int64_t units = (int64_t)NT * MT;
+    const int64_t tiles = (int64_t)NT * MT, units = tiles * splits;
     const int my_tiles = units > (int64_t)blockIdx.x ? (int)((units - 1 - blockIdx.x) / gridDim.x + 1) : 0;
-    const int KW = K / kKW, KS = KW * kSlotsPerW, KX = KS * kXPerSlot;
-    auto origin = [&](int i, int &n0, int &m0) {
-        tile_origin((int64_t)blockIdx.x + (int64_t)i * gridDim.x, NT, MT, TM, n0, m0);
+    const int KW_all = K / kKW;
+    // work unit i of this CTA: output tile b and K split z (weight stages
+    // [wb, we)); a split writes its fp32 partial tile, summed afterwards
+    struct Unit {
+        int n0, m0, z, wb, we;
+    };
+    auto unit = [&](int i) {
+        const int64_t u = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;
+        Unit t;
+        t.z = (int)(u / tiles);
+        tile_origin(u - (int64_t)t.z * tiles, NT, MT, TM, t.n0, t.m0);
+        t.wb = (int)((int64_t)t.z * KW_all / splits);
+        t.we = (int)((int64_t)(t.z + 1) * KW_all / splits);
+        return t;
     };
 
     if (threadIdx.x == 0) {
@@ -681,16 +692,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
             int g = 0;
             bool ok = true;
             for (int i = 0; ok && i < my_tiles; ++i) {
-                int n0, m0;
-                origin(i, n0, m0);
-                for (int ws = 0; ws < KW; ++ws, ++g) {
+                const Unit t = unit(i);
+                for (int ws = t.wb; ws < t.we; ++ws, ++g) {
                     const int wsl = g % kNW;
                     if (!mbar_wait(&w_empty[wsl], ((g / kNW) & 1) ^ 1, abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&w_full[wsl], kWStageBytes);
-                    tma_load_2d(wring + wsl * kWStageBytes, &wmap, ws * kWRowBytes, n0, &w_full[wsl]);
+                    tma_load_2d(wring + wsl * kWStageBytes, &wmap, ws * kWRowBytes, t.n0, &w_full[wsl]);
                 }
             }
             // let every issued copy land before the CTA can exit
@@ -701,13 +711,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // the x stages of every tile: producer p takes stages p, p + P, ...
         const int p = warp - kXProducerWarp;
         if (lane == 0 && p < P) {
-            int next = p;  // first stage (counted over all tiles) not issued
+            int next = p;  // first stage (counted over all units) not issued
+            int base = 0;  // x stages of the units before this one
             bool ok = true;
             for (int i = 0; ok && i < my_tiles; ++i) {
-                int n0, m0;
-                origin(i, n0, m0);
+                const Unit t = unit(i);
+                const int KX = (t.we - t.wb) * (kKW / kXK);
                 for (int s = 0; s < KX; ++s) {
-                    const int g = i * KX + s;
+                    const int g = base + s;
                     if (g % P != p) continue;
                     const int xsl = g % kNX;
                     if (!mbar_wait(&x_empty[xsl], ((g / kNX) & 1) ^ 1, abort_flag, err)) {
@@ -717,10 +728,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
 #pragma unroll
                     for (int j = 0; j < kXChunks; ++j)
-                        tma_load_2d(xring + xsl * Cfg.x_stage + j * TM * 128, &xmap, s * kXK + 64 * j, m0,
-                                    &x_full[xsl]);
+                        tma_load_2d(xring + xsl * Cfg.x_stage + j * TM * 128, &xmap, t.wb * kKW + s * kXK + 64 * j,
+                                    t.m0, &x_full[xsl]);
                     next = g + P;
                 }
+                base += KX;
             }
             for (int i = next - kNX; i < next; i += P)
                 if (i >= 0) mbar_drain(&x_full[i % kNX], (i / kNX) & 1);
@@ -730,14 +742,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)TM);
         int asl = 0;
         uint32_t aph = 0;
+        int base = 0;  // x stages of the units before this one
         bool ok = true;
         for (int i = 0; ok && i < my_tiles; ++i) {
+            const Unit t = unit(i);
+            const int KS = (t.we - t.wb) * kSlotsPerW;
             if (!__all_sync(0xffffffffu, mbar_wait(d_empty, (i & 1) ^ 1, abort_flag, err))) break;
             tc_fence_after();
             for (int s = 0; s < KS; ++s) {
 #pragma unroll
                 for (int u = 0; u < kXPerSlot; ++u) {
-                    const int g = (i * KS + s) * kXPerSlot + u;
+                    const int g = base + s * kXPerSlot + u;
                     ok = __all_sync(0xffffffffu, mbar_wait(&x_full[g % kNX], (g / kNX) & 1, abort_flag, err));
                     if (!ok) break;
                 }
@@ -751,13 +766,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kSK / 16; ++kk) {
                         const int chunk = kk >> 2, u = chunk / kXChunks, jj = chunk % kXChunks;
-                        const int g = (i * KS + s) * kXPerSlot + u;
+                        const int g = base + s * kXPerSlot + u;
                         const uint64_t bdesc =
                             smem_desc_k128(xring + (g % kNX) * Cfg.x_stage + jj * TM * 128) + 2 * (kk & 3);
                         mma_f16_ts(d_tmem, a_tmem + asl * kSlotCols + kk * 8, bdesc, idesc, (s | kk) != 0);
                     }
 #pragma unroll
-                    for (int u = 0; u < kXPerSlot; ++u) mma_commit(&x_empty[((i * KS + s) * kXPerSlot + u) % kNX]);
+                    for (int u = 0; u < kXPerSlot; ++u) mma_commit(&x_empty[(base + s * kXPerSlot + u) % kNX]);
                     mma_commit(&a_empty[asl]);
                 }
                 __syncwarp();
@@ -767,6 +782,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
             }
             if (!ok) break;
+            base += KS * kXPerSlot;
             if (elect_one()) mma_commit(d_full);
             __syncwarp();
         }
@@ -779,7 +795,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         uint32_t aph = 0;
         bool ok = true;
         for (int i = 0; ok && i < my_tiles; ++i) {
-            for (int ws = 0; ws < KW && ok; ++ws, ++g) {
+            const Unit t = unit(i);
+            for (int ws = t.wb; ws < t.we && ok; ++ws, ++g) {
                 const int wsl = g % kNW;
                 ok = __all_sync(0xffffffffu, mbar_wait(&w_full[wsl], (g / kNW) & 1, abort_flag, err));
                 if (!ok) break;
@@ -844,8 +861,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int et = threadIdx.x - kPEpiWarp0 * 32;  // 0..127
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         for (int i = 0; i < my_tiles; ++i) {
-            int n0, m0;
-            origin(i, n0, m0);
+            const Unit t = unit(i);
+            const int n0 = t.n0, m0 = t.m0;
+            float *out = splits > 1 ? part + (size_t)t.z * M * N : nullptr;  // a split's fp32 partial tile
             // the tile's x-row scales (buffer i % 2: the other warps may
             // still read the previous tile's)
             float *xs = xs2 + (i & 1) * scale_rows;
@@ -870,8 +888,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int m = m0 + c + j;
-                    if (c + j < TM && m < M && n < N)
-                        store_y(y, (int64_t)m * N + n, __uint_as_float(v[j]) * sc[j], ybf16 != 0);
+                    if (c + j < TM && m < M && n < N) {
+                        const float val = __uint_as_float(v[j]) * sc[j];
+                        if (out)
+                            out[(int64_t)m * N + n] = val;
+                        else
+                            store_y(y, (int64_t)m * N + n, val, ybf16 != 0);
+                    }
                 }
             }
             tc_fence_before();
@@ -967,14 +990,15 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
         auto pk = gemm_persistent_kernel<kNXShort, 128, 64>;
         e = ensure_smem_attr(reinterpret_cast<const void *>(pk), (int)Cfg.smem);
         if (e != cudaSuccess) return e;
-        return launch_pdl(pk, dim3((unsigned)sms), dim3(kPThreads), Cfg.smem, s, xmap, wmap, y, xscale, (int)M,
-                          (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
+        e = launch_pdl(pk, dim3((unsigned)sms), dim3(kPThreads), Cfg.smem, s, xmap, wmap, y,
+                       splits > 1 ? part : nullptr, xscale, (int)M, (int)N, (int)K, TM, splits, ybf16 ? 1 : 0, err);
+    } else {
+        e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
+        if (e != cudaSuccess) return e;
+        const dim3 grid((unsigned)tiles, 1, (unsigned)splits);
+        e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr,
+                       xscale, (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
     }
-    e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)tiles, 1, (unsigned)splits);
-    e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr, xscale,
-                   (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
     if (e != cudaSuccess || splits == 1) return e;
     const int64_t n4 = M * N / 4;
     return launch_pdl(splitk_reduce_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, s,

@@ -468,13 +468,13 @@ def test_gemm_whole_waves_and_a_ragged_wave(M, K):
 
 def test_gemm_plan():
     """The launch plan the library reports for the prefill shapes: 256-row
-    tiles run persistent at M = 2048 (QKV, O, gate+up) and split at down;
-    M = 272 is one tall tile; small M runs one CTA per tile."""
+    tiles run persistent at M = 2048 (QKV, O, gate+up unsplit, down with K
+    split); M = 272 is one tall tile; small M runs one CTA per tile."""
     q4 = lib()
     p = q4.gemm_plan(2048, 7168, 5120)
     assert p == {"tile_rows": 256, "splits": 1, "persistent": True}
     p = q4.gemm_plan(2048, 5120, 17408)
-    assert p["tile_rows"] == 256 and p["splits"] > 1 and not p["persistent"]
+    assert p["tile_rows"] == 256 and p["splits"] > 1 and p["persistent"]
     p = q4.gemm_plan(272, 34816, 5120)
     assert p == {"tile_rows": 272, "splits": 1, "persistent": False}
     assert not q4.gemm_plan(96, 5120, 5120)["persistent"]
@@ -500,4 +500,20 @@ def test_persistent_gemm_every_output():
     assert torch.equal(q4.matmul(xd, wd, N, K), y)
     y16 = q4.matmul(xd, wd, N, K, out_dtype=torch.bfloat16)
     assert torch.equal(y16, y.to(torch.bfloat16))
+    assert q4.device_error() == 0
+
+
+def test_persistent_gemm_split_k():
+    """The persistent GEMM over (tile, K split) units: the down shape at
+    M = 1000 (four 256-row x tiles, K split four ways): sampled outputs
+    against the oracle, bitwise repeatable."""
+    q4 = lib()
+    M, N, K = 1000, 5120, 17408
+    p = q4.gemm_plan(M, N, K)
+    assert p["persistent"] and p["splits"] > 1, p
+    x, wq = case(9800, M, N, K, outlier_blocks=0.05, act_outliers=0.01)
+    xd, wd = x_dev(x), wq_dev(wq)
+    y = q4.gemm(xd, wd, N, K)
+    check_sampled(y, x, wq, N, K, seed=3)
+    assert torch.equal(q4.gemm(xd, wd, N, K), y)
     assert q4.device_error() == 0
