@@ -115,12 +115,12 @@ struct GemmLayout {
     }
 };
 
-// The persistent form runs tiles of 193..256 rows (one MMA wide, 128-k slots
-// fed by 64-k x chunks) when there are at least two work units (tiles times
-// K splits) per SM.
+// The persistent form runs the tiles with 128-k A slots (more than 128
+// rows, one CTA per SM) when there are more work units (tiles times K
+// splits) than SMs, so that some CTA takes two or more.
 bool use_persistent(int tm, int nx, int64_t tiles, int splits, int sms) {
-    return tm > kWideSlotMaxRows && tm <= kMaxTileRowsShort && nx == kNXShort && slot_k(tm) == 128 &&
-           xstage_k(tm) == 64 && sms > 0 && tiles * splits >= 2 * (int64_t)sms;
+    return slot_k(tm) == 128 && (nx == kNXShort || nx == kNXMid || nx == kNXTall) && sms > 0 &&
+           tiles * splits > (int64_t)sms;
 }
 
 // x ring depth for a tile of tm rows when the launch has `ctas` CTAs on
@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kPThreads = 384;
 constexpr int kPEpiWarp0 = 8;
 
-template <int kNX, int kSK, int kXK>
+template <bool kTall, int kNX, int kSK, int kXK>
 __global__ void __launch_bounds__(kPThreads, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                            float *__restrict__ y, float *__restrict__ part, const float *__restrict__ xscale, int M,
@@ -727,9 +727,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     }
                     mbar_arrive_expect_tx(&x_full[xsl], Cfg.x_stage);
 #pragma unroll
-                    for (int j = 0; j < kXChunks; ++j)
-                        tma_load_2d(xring + xsl * Cfg.x_stage + j * TM * 128, &xmap, t.wb * kKW + s * kXK + 64 * j,
-                                    t.m0, &x_full[xsl]);
+                    for (int j = 0; j < kXChunks; ++j) {
+                        const int kx = t.wb * kKW + s * kXK + 64 * j;
+                        uint8_t *dst = xring + xsl * Cfg.x_stage + j * TM * 128;
+                        tma_load_2d(dst, &xmap, kx, t.m0, &x_full[xsl]);
+                        if (kTall)  // a TMA box is at most 256 rows: two boxes of TM / 2
+                            tma_load_2d(dst + (TM / 2) * 128, &xmap, kx, t.m0 + TM / 2, &x_full[xsl]);
+                    }
                     next = g + P;
                 }
                 base += KX;
@@ -739,7 +743,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else if (warp == 1) {
         // MMA issue; tile i waits until the epilogue has read tile i - 1
-        const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)TM);
+        const uint32_t idesc = idesc_f16_f32(kTileN, (uint32_t)(kTall ? 256 : TM));
+        const uint32_t idesc2 = idesc_f16_f32(kTileN, (uint32_t)(kTall ? TM - 256 : 16));
         int asl = 0;
         uint32_t aph = 0;
         int base = 0;  // x stages of the units before this one
@@ -769,7 +774,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         const int g = base + s * kXPerSlot + u;
                         const uint64_t bdesc =
                             smem_desc_k128(xring + (g % kNX) * Cfg.x_stage + jj * TM * 128) + 2 * (kk & 3);
-                        mma_f16_ts(d_tmem, a_tmem + asl * kSlotCols + kk * 8, bdesc, idesc, (s | kk) != 0);
+                        const uint32_t acol = a_tmem + asl * kSlotCols + kk * 8;
+                        mma_f16_ts(d_tmem, acol, bdesc, idesc, (s | kk) != 0);
+                        if (kTall)  // rows 256.. start 256 x 128 bytes into the chunk
+                            mma_f16_ts(d_tmem + 256, acol, bdesc + (256 * 128 >> 4), idesc2, (s | kk) != 0);
                     }
 #pragma unroll
                     for (int u = 0; u < kXPerSlot; ++u) mma_commit(&x_empty[(base + s * kXPerSlot + u) % kNX]);
@@ -986,8 +994,11 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
     const int64_t tiles = ((N + kTileN - 1) / kTileN) * ((M + TM - 1) / TM);
     const int sms = device_sm_count(dev);
     if (use_persistent(TM, nx, tiles, splits, sms)) {
-        // many 256-row tiles: the persistent form (one CTA per SM)
-        auto pk = gemm_persistent_kernel<kNXShort, 128, 64>;
+        // more work units than SMs: the persistent form (one CTA per SM)
+        using PK = decltype(&gemm_persistent_kernel<false, kNXShort, 128, 64>);
+        const PK pk = TM > kMaxTileRowsShort ? gemm_persistent_kernel<true, kNXTall, 128, 128>
+                      : nx == kNXMid         ? gemm_persistent_kernel<false, kNXMid, 128, 128>
+                                             : gemm_persistent_kernel<false, kNXShort, 128, 64>;
         e = ensure_smem_attr(reinterpret_cast<const void *>(pk), (int)Cfg.smem);
         if (e != cudaSuccess) return e;
         e = launch_pdl(pk, dim3((unsigned)sms), dim3(kPThreads), Cfg.smem, s, xmap, wmap, y,

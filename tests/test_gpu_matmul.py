@@ -469,14 +469,15 @@ def test_gemm_whole_waves_and_a_ragged_wave(M, K):
 def test_gemm_plan():
     """The launch plan the library reports for the prefill shapes: 256-row
     tiles run persistent at M = 2048 (QKV, O, gate+up unsplit, down with K
-    split); M = 272 is one tall tile; small M runs one CTA per tile."""
+    split); M = 272 is one tall tile, persistent for gate+up (more tiles
+    than SMs); small M runs one CTA per tile."""
     q4 = lib()
     p = q4.gemm_plan(2048, 7168, 5120)
     assert p == {"tile_rows": 256, "splits": 1, "persistent": True}
     p = q4.gemm_plan(2048, 5120, 17408)
     assert p["tile_rows"] == 256 and p["splits"] > 1 and p["persistent"]
     p = q4.gemm_plan(272, 34816, 5120)
-    assert p == {"tile_rows": 272, "splits": 1, "persistent": False}
+    assert p == {"tile_rows": 272, "splits": 1, "persistent": True}
     assert not q4.gemm_plan(96, 5120, 5120)["persistent"]
     with pytest.raises(q4.Q4Error):
         q4.gemm_plan(64, 128, 300)

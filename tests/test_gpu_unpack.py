@@ -187,6 +187,25 @@ def test_one_hot_persistent_gemm():
     assert_exact(Y, E, 1.0, [0], K, K, "persistent GEMM")
     assert q4.device_error() == 0
 
+
+def test_one_hot_persistent_tall_gemm():
+    """x = v I through tall x tiles (M = 272, a second MMA per k step) with
+    more weight tiles than SMs, so that the persistent form runs: every
+    (n, k) equals RN16(w) v exactly."""
+    q4 = lib()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N, K, M = 128 * (sms + 8) + 40, 1024, 272
+    p = q4.gemm_plan(M, N, K)
+    assert p["persistent"] and p["tile_rows"] == 272, p
+    wq = q4_matrix(16, N, K)
+    wd = wq_dev(wq)
+    E = expected(wq, N, K, rounded16=True)
+    X = one_hot_x(K, -0.75)
+    rows = starts(K, M)
+    Y = run_rows(lambda xs: q4.gemm(xs, wd, N, K), X, rows, N, K, M)
+    assert_exact(Y, E, -0.75, rows, M, K, "persistent tall GEMM")
+    assert q4.device_error() == 0
+
 def test_scale_classes_present():
     """The test matrices hold every scale class the kernels distinguish."""
     o = oracle.get()
