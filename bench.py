@@ -396,7 +396,7 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
         # fraction beside it
         roof = {"bound": "tensor", "achieved": round(tflops / world, 1), "peak": tf_burst,
                 "unit": "TFLOP/s", "frac": round(tflops / world / tf_burst, 4), "traffic": None,
-                "kernel": dominant_kernel(M), "peak_source": peak_kind + " bf16 burst (kind::f16 runs at the bf16 rate)",
+                "kernel": dominant_kernel(M, q4=q4), "peak_source": peak_kind + " bf16 burst (kind::f16 runs at the bf16 rate)",
                 "frac_of_sustained": round(tflops / world / tf_sust, 4), "peak_sustained": tf_sust,
                 "flops_per_launch": round(step_flops / calls_per_step),
                 "avg_launch_us": round(ms_local * 1e3 / calls, 3),
@@ -499,6 +499,8 @@ def workload_name(w, M, layers, grouped=False):
 
 # q4_0_matmul sends M up to this to the decode kernels, larger M to the GEMM
 DECODE_MAX_M = 64
+# gate+up, the largest matrix of a layer (N, K): its GEMM plan names the prefill kernel
+SHAPES_FOR_PLAN = (34816, 5120)
 
 
 def kernels_per_call(q4, M, N, K):
@@ -514,13 +516,22 @@ def kernels_per_call(q4, M, N, K):
     return 3 if q4.lib().q4_0_gemm_workspace_bytes(M, N, K) > x16 else 2
 
 
-def dominant_kernel(M, grouped=False):
+def dominant_kernel(M, grouped=False, q4=None):
     if grouped:
         return f"gemv_dp4a_grouped_kernel<{M}>"
     if M <= 2:
         return f"gemv_dp4a_kernel<{M}>"
     if M <= DECODE_MAX_M:
         return f"gemv_tc_kernel<{16 if M <= 16 else (32 if M <= 32 else 64)}>"
+    # the largest matrix of the step (gate+up) decides: one CTA per tile, or
+    # the persistent form (the library's launch plan)
+    if q4 is not None:
+        N, K = SHAPES_FOR_PLAN
+        try:
+            if q4.gemm_plan(M, N, K)["persistent"]:
+                return "gemm_persistent_kernel"
+        except Exception:
+            pass
     return "gemm_kernel"
 
 
