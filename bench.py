@@ -346,7 +346,15 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
     h2d = sum(x.numel() * 2 for x in x_host) * (layers if sweep else 1)
     d2h = sum(y.numel() * ysz for y in y_host) * (layers if sweep else 1)
 
-    def e2e_step(i):
+    # where an e2e step's time goes: host time inside the library calls,
+    # device time of the step (events around it), and the wait for it
+    parts_t = {"api": 0.0, "sync": 0.0, "device": 0.0}
+    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step(i, account=False):
+        t_a = time.perf_counter()
+        if account:
+            ev_a.record(stream)
         ls = range(layers) if sweep else (i % layers,)
         for l in ls:
             if grouped:
@@ -362,7 +370,14 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
                 for p, (m0, m1) in enumerate(parts):
                     q4.matmul_host(x_host[j][m0:m1], wq[l][j], N, K, out=y_host[j][m0:m1], workspace=whs[j][p],
                                    stream=stream, out_dtype=ydt)
+        if account:
+            ev_b.record(stream)
+        t_b = time.perf_counter()
         stream.synchronize()
+        if account:
+            parts_t["api"] += t_b - t_a
+            parts_t["sync"] += time.perf_counter() - t_b
+            parts_t["device"] += ev_a.elapsed_time(ev_b) / 1e3
 
     with torch.cuda.stream(stream):
         for i in range(min(3, e2e_steps)):  # first calls of the host path outside the timing
@@ -372,7 +387,7 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(e2e_steps):
-            e2e_step(i)
+            e2e_step(i, account=True)
     t_e2e = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
     tensor_bound = M >= 256
@@ -410,7 +425,12 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
            "tok_s_eq": round(tok_s, 1), "tflops": round(tflops, 2), "gbs": round(gbs, 1),
            "gpu_launches": launches, "roofline": roof, "clocks": clk,
            "e2e": {"value": round(e2e_val, 2), "unit": unit, "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                   "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                   "us_per_step": round(t_e2e / e2e_steps * 1e6, 2),
+                   "breakdown_us_per_step": {
+                       "host_in_library_calls": round(parts_t["api"] / e2e_steps * 1e6, 2),
+                       "waiting_for_the_step": round(parts_t["sync"] / e2e_steps * 1e6, 2),
+                       "device_time_of_the_step": round(parts_t["device"] / e2e_steps * 1e6, 2)}},
            "layer_copies": layers,
            "graphs": " + ".join(f"{reps} x {n} steps" for _, n, reps in plan)}
     if cpu:
