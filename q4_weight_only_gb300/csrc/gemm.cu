@@ -259,8 +259,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__rest
 __device__ __forceinline__ bool scale_is_large(uint32_t dbits) { return (dbits & 0x7C00u) >= 0x1400u; }
 
 template <bool kAnyScale>
-__device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q)[4], uint32_t *out) {
-    const uint32_t kBias = 0x64006400u;                         // (1024, 1024)
+__device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q)[4], uint32_t *out,
+                                              uint32_t kBias /* kNibbleBias, as a register */) {
     const half2 k1032 = u2h(0x64086408u), k1152 = u2h(0x64806480u);
     const half2 d2 = u2h(dbits * 0x00010001u);                  // (d, d)
     if (!kAnyScale) {
@@ -268,20 +268,20 @@ __device__ __forceinline__ void dequant_block(uint32_t dbits, const uint32_t (&Q
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
             const uint32_t q = Q[wi], t = __umulhi(q, 1u << 24);  // t = q >> 8
-            out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x000F000Fu) | kBias), k1032), d2));
-            out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x000F000Fu) | kBias), k1032), d2));
-            out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x00F000F0u) | kBias), k1152), d16));
-            out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x00F000F0u) | kBias), k1152), d16));
+            out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(q, kBias)), k1032), d2));
+            out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(t, kBias)), k1032), d2));
+            out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(and_or<0x00F000F0u>(q, kBias)), k1152), d16));
+            out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(and_or<0x00F000F0u>(t, kBias)), k1152), d16));
         }
         return;
     }
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
         const uint32_t q = Q[wi], t = q >> 8;
-        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x000F000Fu) | kBias), k1032), d2));
-        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x000F000Fu) | kBias), k1032), d2));
-        out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(((q >> 4) & 0x000F000Fu) | kBias), k1032), d2));
-        out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(((t >> 4) & 0x000F000Fu) | kBias), k1032), d2));
+        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(q, kBias)), k1032), d2));
+        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(t, kBias)), k1032), d2));
+        out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(q >> 4, kBias)), k1032), d2));
+        out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(t >> 4, kBias)), k1032), d2));
     }
 }
 
@@ -306,7 +306,7 @@ template <bool kTall, int kNX, int kSK, int kXK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 float *__restrict__ y, float *__restrict__ part, const float *__restrict__ xscale, int M, int N,
-                int K, int TM, int ybf16, unsigned int *err) {
+                int K, int TM, int ybf16, uint32_t nib_bias, unsigned int *err) {
     constexpr int kChunks = kSK / 64;         // 64-k pieces per slot (A stores)
     constexpr int kXPerSlot = kSK / kXK;      // x stages per A slot
     constexpr int kXChunks = kXK / 64;        // 64-k chunks (TMA boxes) per x stage
@@ -519,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 __funnelshift_r(wv[3], wv[4], 16)};
                         const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
                         uint32_t cols[32];
-                        dequant_block<kAny>(wv[0] & 0xFFFFu, Q0, cols);
-                        dequant_block<kAny>(wv[4] >> 16, Q1, cols + 16);
+                        dequant_block<kAny>(wv[0] & 0xFFFFu, Q0, cols, nib_bias);
+                        dequant_block<kAny>(wv[4] >> 16, Q1, cols + 16, nib_bias);
                         tmem_st32(a_tmem + lane_base + asl * kSlotCols + pc * 32, cols);
                     }
                     tmem_wait_st();
@@ -611,7 +611,8 @@ template <bool kTall, int kNX, int kSK, int kXK>
 __global__ void __launch_bounds__(kPThreads, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                            float *__restrict__ y, float *__restrict__ part, const float *__restrict__ xscale, int M,
-                           int N, int K, int TM, int splits, int ybf16, unsigned int *err) {
+                           int N, int K, int TM, int splits, int ybf16, uint32_t nib_bias,
+                           unsigned int *err) {
     constexpr int kChunks = kSK / 64;
     constexpr int kXPerSlot = kSK / kXK;
     constexpr int kXChunks = kXK / 64;
@@ -838,8 +839,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                                     __funnelshift_r(wv[3], wv[4], 16)};
                             const uint32_t Q1[4] = {wv[5], wv[6], wv[7], wv[8]};
                             uint32_t cols[32];
-                            dequant_block<kAny>(wv[0] & 0xFFFFu, Q0, cols);
-                            dequant_block<kAny>(wv[4] >> 16, Q1, cols + 16);
+                            dequant_block<kAny>(wv[0] & 0xFFFFu, Q0, cols, nib_bias);
+                            dequant_block<kAny>(wv[4] >> 16, Q1, cols + 16, nib_bias);
                             tmem_st32(a_tmem + lane_base + asl * kSlotCols + pc * 32, cols);
                         }
                         tmem_wait_st();
@@ -1002,13 +1003,14 @@ cudaError_t launch_tm(int TM, int splits, const void *x16, const float *xscale, 
         e = ensure_smem_attr(reinterpret_cast<const void *>(pk), (int)Cfg.smem);
         if (e != cudaSuccess) return e;
         e = launch_pdl(pk, dim3((unsigned)sms), dim3(kPThreads), Cfg.smem, s, xmap, wmap, y,
-                       splits > 1 ? part : nullptr, xscale, (int)M, (int)N, (int)K, TM, splits, ybf16 ? 1 : 0, err);
+                       splits > 1 ? part : nullptr, xscale, (int)M, (int)N, (int)K, TM, splits, ybf16 ? 1 : 0, kNibbleBias,
+                       err);
     } else {
         e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)Cfg.smem);
         if (e != cudaSuccess) return e;
         const dim3 grid((unsigned)tiles, 1, (unsigned)splits);
         e = launch_pdl(kernel, grid, dim3(kThreads), Cfg.smem, s, xmap, wmap, y, splits > 1 ? part : nullptr,
-                       xscale, (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, err);
+                       xscale, (int)M, (int)N, (int)K, TM, ybf16 ? 1 : 0, kNibbleBias, err);
     }
     if (e != cudaSuccess || splits == 1) return e;
     const int64_t n4 = M * N / 4;

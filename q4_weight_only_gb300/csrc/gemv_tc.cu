@@ -99,8 +99,8 @@ __device__ __forceinline__ uint32_t h2u(half2 h) { return *reinterpret_cast<uint
 __device__ __forceinline__ bool scale_is_large(uint32_t dbits) { return (dbits & 0x7C00u) >= 0x1400u; }
 
 template <bool kAnyScale>
-__device__ __forceinline__ void dequant_block16(uint32_t dbits, const uint32_t (&Q)[4], uint32_t (&out)[16]) {
-    const uint32_t kBias = 0x64006400u;                         // (1024, 1024)
+__device__ __forceinline__ void dequant_block16(uint32_t dbits, const uint32_t (&Q)[4], uint32_t (&out)[16],
+                                                uint32_t kBias /* kNibbleBias, as a register */) {
     const half2 k1032 = u2h(0x64086408u), k1152 = u2h(0x64806480u);
     const half2 d2 = u2h(dbits * 0x00010001u);                  // (d, d)
     if (!kAnyScale) {
@@ -108,20 +108,20 @@ __device__ __forceinline__ void dequant_block16(uint32_t dbits, const uint32_t (
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
             const uint32_t q = Q[wi], t = __umulhi(q, 1u << 24);  // t = q >> 8
-            out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x000F000Fu) | kBias), k1032), d2));
-            out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x000F000Fu) | kBias), k1032), d2));
-            out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x00F000F0u) | kBias), k1152), d16));
-            out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x00F000F0u) | kBias), k1152), d16));
+            out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(q, kBias)), k1032), d2));
+            out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(t, kBias)), k1032), d2));
+            out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(and_or<0x00F000F0u>(q, kBias)), k1152), d16));
+            out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(and_or<0x00F000F0u>(t, kBias)), k1152), d16));
         }
         return;
     }
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
         const uint32_t q = Q[wi], t = q >> 8;
-        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h((q & 0x000F000Fu) | kBias), k1032), d2));
-        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h((t & 0x000F000Fu) | kBias), k1032), d2));
-        out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(((q >> 4) & 0x000F000Fu) | kBias), k1032), d2));
-        out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(((t >> 4) & 0x000F000Fu) | kBias), k1032), d2));
+        out[2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(q, kBias)), k1032), d2));
+        out[2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(t, kBias)), k1032), d2));
+        out[8 + 2 * wi + 0] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(q >> 4, kBias)), k1032), d2));
+        out[8 + 2 * wi + 1] = h2u(__hmul2(__hsub2(u2h(and_or<0x000F000Fu>(t >> 4, kBias)), k1032), d2));
     }
 }
 
@@ -228,7 +228,8 @@ template <int TM>
 __global__ void __launch_bounds__(kThreads, 2)
     gemv_tc_kernel(const uint4 *__restrict__ xt, const __grid_constant__ CUtensorMap wmap,
                    float *__restrict__ y, float *__restrict__ part, unsigned int *__restrict__ tile_cnt,
-                   const float *__restrict__ xscale, int M, int N, int K, int ybf16, unsigned int *err) {
+                   const float *__restrict__ xscale, int M, int N, int K, int ybf16, uint32_t nib_bias,
+                   unsigned int *err) {
     using C = Cfg<TM>;
     constexpr int kNX = C::kNX, kNW = C::kNW;
     extern __shared__ uint8_t smem_raw[];
@@ -405,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         uint32_t cols[32];
                         uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols);
                         uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(cols + 16);
-                        dequant_block16<kAny>(wv[0] & 0xFFFFu, Q0, lo);
-                        dequant_block16<kAny>(wv[4] >> 16, Q1, hi);
+                        dequant_block16<kAny>(wv[0] & 0xFFFFu, Q0, lo, nib_bias);
+                        dequant_block16<kAny>(wv[4] >> 16, Q1, hi, nib_bias);
                         tmem_st32(a_tmem + lane_base + asl * (kKB / 2) + j * 32, cols);
                     }
                 };
@@ -625,7 +626,7 @@ cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16
     if (e != cudaSuccess) return e;
     return launch_pdl(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads), C::kSmem, s,
                       reinterpret_cast<const uint4 *>(ws), wmap, y, part, cnt, static_cast<const float *>(xscale),
-                      (int)M, (int)N, (int)K, ybf16 ? 1 : 0, err);
+                      (int)M, (int)N, (int)K, ybf16 ? 1 : 0, kNibbleBias, err);
 }
 
 }  // namespace

@@ -190,6 +190,24 @@ __device__ __forceinline__ void store_y(float *y, int64_t i, float v, bool bf16)
         y[i] = v;
 }
 
+// ------------------------------------------------- nibble unpack helper
+
+// (q & kMask) | bias in one LOP3.  A LOP3 takes at most one immediate
+// operand, so a constant mask and a constant bias together compile to two
+// instructions; the kernels therefore receive the bias as a kernel argument
+// (ptxas cannot fold it) and it reaches the LOP3 as a register.
+template <uint32_t kMask>
+__device__ __forceinline__ uint32_t and_or(uint32_t q, uint32_t bias) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(q), "n"(kMask), "r"(bias));
+    return r;
+}
+
+// The binary16 pair (1024, 1024): the bias that turns a nibble OR-ed into
+// the low mantissa bits into 1024 + q.  Passed to the kernels as an argument
+// (see and_or).
+constexpr uint32_t kNibbleBias = 0x64006400u;
+
 // -------------------------------------------------------------- tcgen05
 
 // Allocate `ncols` (power of two >= 32) TMEM columns; the base address is
