@@ -294,11 +294,12 @@ int q4_0_gemm(const uint16_t *x, const uint8_t *wq, float *y,
  * default workspace (q4_0_gemm_workspace_bytes) on the current device, and
  * that q4_0_matmul makes for M > 64.  No work is launched.
  *   *tile_rows  : x rows per output tile (a multiple of 16, at most 320)
- *   *splits     : ways K is split over CTAs (1..4; partial tiles summed in
- *                 split order afterwards)
- *   *persistent : 1 when one CTA per SM takes several tiles in turn (tiles of
- *                 193..256 rows, at least two tiles per SM, no split), else
- *                 0 (one CTA per tile)
+ *   *splits     : ways K is split over CTAs (1..4; the fp32 partial tiles
+ *                 are summed in split order by a second kernel afterwards)
+ *   *persistent : 1 when one CTA per SM takes several work units (output
+ *                 tiles, or tile x K-split units) in turn -- tiles of more
+ *                 than 128 rows, more units than SMs -- else 0 (one CTA per
+ *                 tile and split)
  * Errors: Q4_0_ERR_INVALID_ARG for a null output pointer, M, N < 1 or
  * K % 256 != 0; Q4_0_ERR_CUDA when no device is current.
  */

@@ -218,20 +218,26 @@ __global__ void __launch_bounds__(kXThreads, 8) x_to_f16_kernel(const uint4 *__r
 }
 
 // y = sum over splits of the partial tiles, in split order (deterministic);
-// y is fp32, or bfloat16 rounded to nearest even when ybf16.
+// y is fp32, or bfloat16 rounded to nearest even when ybf16.  A thread's
+// loads of all splits (at most four) are issued before the first add, so
+// it pays one L2 round trip rather than one per split.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__restrict__ part, float *__restrict__ y,
                                                             int64_t n4, int splits, int ybf16) {
     pdl_launch_dependents();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
-    float4 acc = part[i];
-    for (int z = 1; z < splits; ++z) {
-        const float4 v = part[(int64_t)z * n4 + i];
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+    float4 v[4];
+#pragma unroll
+    for (int z = 0; z < 4; ++z) v[z] = z < splits ? __ldcg(part + (int64_t)z * n4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = v[0];
+#pragma unroll
+    for (int z = 1; z < 4; ++z) {
+        if (z >= splits) break;
+        acc.x += v[z].x;
+        acc.y += v[z].y;
+        acc.z += v[z].z;
+        acc.w += v[z].w;
     }
     if (ybf16) {
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
