@@ -1035,11 +1035,27 @@ int64_t xscale_bytes(int64_t M) { return (M * 4 + 255) / 256 * 256; }
 // Rows of x per CTA tile.  Each extra tile dequantises every weight tile
 // once more, but tiles of more than 256 rows run with a shallower x ring:
 // they are used when they need at most three quarters as many tiles as
-// 256-row ones (M = 272: one tile instead of two; M = 2048 stays at eight
-// of 256).  Then the smallest multiple of 16 that covers M in that many.
-int tile_rows(int64_t M) {
+// 256-row ones (M = 272: one tile instead of two).  From four 256-row
+// tiles up (M > 768), when both tilings give every SM at least one tile (so
+// K is not split) and `sms` is known, whole waves decide instead: a wave
+// costs its tile height plus about 100 rows'
+// worth of MMA time for the tile's own work (its weight tile's
+// dequantisation, the epilogue), and tall tiles are taken when that saves
+// more than 5 % (the O and down projections at M = 2048: seven tiles of 304
+// rows, 280 tiles on 152 SMs in two waves, instead of eight of 256, 320
+// tiles in three).  Then the smallest multiple of 16 that covers M in that
+// many tiles.
+int tile_rows(int64_t M, int64_t N, int sms) {
     const int64_t t256 = (M + 255) / 256, tall = (M + kMaxTileRows - 1) / kMaxTileRows;
-    const int64_t tiles_m = 4 * tall <= 3 * t256 ? tall : t256;
+    int64_t tiles_m = 4 * tall <= 3 * t256 ? tall : t256;
+    const int64_t nt = (N + kTileN - 1) / kTileN;
+    if (sms > 0 && t256 >= 4 && tall < t256 && tall * nt >= sms) {
+        auto cost = [&](int64_t tm_count) {
+            const int64_t rows = ((M + tm_count - 1) / tm_count + 15) / 16 * 16;
+            return (double)((tm_count * nt + sms - 1) / sms) * (double)(rows + 100);
+        };
+        tiles_m = cost(tall) < 0.95 * cost(t256) ? tall : t256;
+    }
     return (int)(((M + tiles_m - 1) / tiles_m + 15) / 16 * 16);
 }
 
@@ -1051,7 +1067,8 @@ int tile_rows(int64_t M) {
 // (2 * M * N * K flops at about 1 PFLOP/s): about 600 * S / K.  Each split
 // keeps at least two weight stages.
 int gemm_splits(int64_t M, int64_t N, int64_t K, int sms) {
-    const int64_t ctas = ((N + kTileN - 1) / kTileN) * ((M + tile_rows(M) - 1) / tile_rows(M));
+    const int tm = tile_rows(M, N, sms);
+    const int64_t ctas = ((N + kTileN - 1) / kTileN) * ((M + tm - 1) / tm);
     if (sms <= 0 || ctas <= 0 || (M * N) % 4 != 0) return 1;
     int best = 1;
     double best_score = 0.0;
@@ -1072,12 +1089,12 @@ int gemm_splits(int64_t M, int64_t N, int64_t K, int sms) {
 // one CTA per row of x.
 bool gemm_shape_supported(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 1) return false;
-    const int tm = tile_rows(M);
+    const int tm = tile_rows(M, N, 0);  // the most tiles any device's choice gives
     return ((N + kTileN - 1) / kTileN) * ((M + tm - 1) / tm) <= 0x7FFFFFFF && M <= 0x7FFFFFFF;
 }
 
 void gemm_plan(int64_t M, int64_t N, int64_t K, int sms, int splits, int *tile_rows_out, int *persistent_out) {
-    const int tm = tile_rows(M);
+    const int tm = tile_rows(M, N, sms);
     const int64_t tiles = ((N + kTileN - 1) / kTileN) * ((M + tm - 1) / tm);
     const int nx = x_ring_stages(tm, tiles * splits, sms);
     *tile_rows_out = tm;
@@ -1101,7 +1118,11 @@ cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf
                                reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(x16), xscale,
                                (int)(K / 8));
     if (e != cudaSuccess) return e;
-    return launch_tm(tile_rows(M), splits < 1 ? 1 : splits, x16, xscale, wq, y, ybf16, part, M, N, K, s, err);
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return launch_tm(tile_rows(M, N, device_sm_count(dev)), splits < 1 ? 1 : splits, x16, xscale, wq, y, ybf16,
+                     part, M, N, K, s, err);
 }
 
 }  // namespace q4_0

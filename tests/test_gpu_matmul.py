@@ -467,20 +467,42 @@ def test_gemm_whole_waves_and_a_ragged_wave(M, K):
 
 
 def test_gemm_plan():
-    """The launch plan the library reports for the prefill shapes: 256-row
-    tiles run persistent at M = 2048 (QKV, O, gate+up unsplit, down with K
-    split); M = 272 is one tall tile, persistent for gate+up (more tiles
-    than SMs); small M runs one CTA per tile."""
+    """The launch plan the library reports for the prefill shapes at M =
+    2048: QKV and gate+up in 256-row tiles, O and down (40 weight tiles) in
+    seven tall tiles of 304 rows -- 280 tiles, two waves on 152 SMs, instead
+    of 320 in three -- all persistent and unsplit; M = 272 is one tall
+    tile, persistent for gate+up (more tiles than SMs); small M runs one CTA
+    per tile."""
     q4 = lib()
     p = q4.gemm_plan(2048, 7168, 5120)
     assert p == {"tile_rows": 256, "splits": 1, "persistent": True}
-    p = q4.gemm_plan(2048, 5120, 17408)
-    assert p["tile_rows"] == 256 and p["splits"] > 1 and p["persistent"]
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        for K in (5120, 17408):
+            p = q4.gemm_plan(2048, 5120, K)
+            assert p == {"tile_rows": 304, "splits": 1, "persistent": True}, p
     p = q4.gemm_plan(272, 34816, 5120)
     assert p == {"tile_rows": 272, "splits": 1, "persistent": True}
     assert not q4.gemm_plan(96, 5120, 5120)["persistent"]
     with pytest.raises(q4.Q4Error):
         q4.gemm_plan(64, 128, 300)
+
+
+def test_gemm_wave_aware_tall_tiles_every_output():
+    """M = 2048 against 40 weight tiles takes seven tall x tiles (six of
+    304 rows and a ragged one of 224) in the persistent form: every output
+    against the oracle, bitwise repeatable, and equal to the same call made
+    through q4_0_matmul."""
+    q4 = lib()
+    M, N, K = 2048, 5120, 1024
+    p = q4.gemm_plan(M, N, K)
+    assert p["tile_rows"] > 256 and p["persistent"] and p["splits"] == 1, p
+    x, wq = case(9900, M, N, K, outlier_blocks=0.05)
+    xd, wd = x_dev(x), wq_dev(wq)
+    y = q4.gemm(xd, wd, N, K)
+    check_full(y, x, wq, N, K)
+    assert torch.equal(q4.gemm(xd, wd, N, K), y)
+    assert torch.equal(q4.matmul(xd, wd, N, K), y)
+    assert q4.device_error() == 0
 
 
 def test_persistent_gemm_every_output():
