@@ -154,29 +154,59 @@ __device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 u) {
 // position c ^ (m & 7) (the 128-byte swizzle named in the MMA's shared-memory
 // descriptor), values in the k order of the weight tiles; rows m >= M are
 // zero.  One CTA per row of the tile: the row's maximum, then the
-// conversion of the chunks the threads still hold in registers (rows longer
-// than 8192 reload the rest).  128 threads of at most 56 registers, so that
-// its CTAs fit beside two CTAs of the running decode kernel and start as
-// soon as it completes.
+// conversion of the chunks the threads still hold in registers.  Rows of
+// 8192 < K <= 24576 are first brought into shared memory by bulk copies
+// (one round trip; with a thread's chunks beyond the eight it holds
+// re-read from L2 in each pass, the K = 17408 pre-pass had cost about 2 us
+// more per call); longer rows reload the rest.  128 threads of at most 56
+// registers (and at most 48 KB of shared memory), so that its CTAs fit
+// beside two CTAs of the running decode kernel and start as soon as it
+// completes.
 constexpr int kXThreads = 128;
 constexpr int kXHeld = 8;  // chunks per thread kept in registers between the passes (K <= 8192)
+constexpr int kXStagedMaxK = 24576;  // rows staged in shared memory: K * 2 bytes <= 48 KB
+__host__ __device__ constexpr bool x_row_staged(int64_t K) { return K > kXHeld * 8 * kXThreads && K <= kXStagedMaxK; }
 template <int TM>
 __global__ void __launch_bounds__(kXThreads, 9) x_tiles_kernel(const uint16_t *__restrict__ x, uint4 *__restrict__ xt,
                                                             float *__restrict__ xscale, int M, int K,
-                                                            unsigned int *__restrict__ tile_cnt, int ncnt) {
+                                                            unsigned int *__restrict__ tile_cnt, int ncnt,
+                                                            unsigned int *err) {
+    extern __shared__ __align__(16) uint4 xrow[];  // the staged row (x_row_staged(K))
+    __shared__ uint64_t xbar;
+    __shared__ int xabort;
     pdl_launch_dependents();
+    const int m = blockIdx.x;
+    const int kc8 = K / 8;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)m * K);
+    const bool staged = x_row_staged(K);
+    if (staged && threadIdx.x == 0) {
+        mbar_init(&xbar, 1);
+        xabort = 0;
+        mbar_fence_init();
+    }
     pdl_wait();  // x may come from the previous kernel (and the last one has read its counters)
     if (blockIdx.x == 0)  // the split-K tile counters of the matmul kernel that follows
         for (int i = threadIdx.x; i < ncnt; i += kXThreads) tile_cnt[i] = 0u;
     __shared__ uint32_t wmax[kXThreads / 32];
-    const int m = blockIdx.x;
-    const int kc8 = K / 8;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)m * K);
     uint4 held[kXHeld];
 #pragma unroll
     for (int h = 0; h < kXHeld; ++h) held[h] = make_uint4(0, 0, 0, 0);
     uint32_t mb = 0;
-    if (m < M) {
+    if (staged) {
+        __syncthreads();  // the barrier's initialisation
+        if (m < M) {
+            if (threadIdx.x == 0) {
+                const uint32_t bytes = (uint32_t)K * 2;
+                mbar_arrive_expect_tx(&xbar, bytes);
+                for (uint32_t off = 0; off < bytes; off += 16384)
+                    bulk_g2s(reinterpret_cast<uint8_t *>(xrow) + off, reinterpret_cast<const uint8_t *>(src) + off,
+                             bytes - off < 16384 ? bytes - off : 16384, &xbar);
+            }
+            const bool ok = mbar_wait(&xbar, 0, &xabort, err);
+            for (int kc = threadIdx.x; ok && kc < kc8; kc += kXThreads) mb = max(mb, bf16x8_absmax_bits(xrow[kc]));
+            if (!ok) mbar_drain(&xbar, 0);  // the copies land before the CTA can exit
+        }
+    } else if (m < M) {
 #pragma unroll
         for (int h = 0; h < kXHeld; ++h) {
             const int kc = threadIdx.x + h * kXThreads;
@@ -215,6 +245,11 @@ __global__ void __launch_bounds__(kXThreads, 9) x_tiles_kernel(const uint16_t *_
         const int u4 = kc >> 5, a = (kc >> 3) & 3, c = kc & 7;
         xt[((int64_t)(u4 * 4 + a) * TM + m) * 8 + (c ^ (m & 7))] = v;
     };
+    if (staged) {
+        for (int kc = threadIdx.x; kc < kc8; kc += kXThreads)
+            store(kc, m < M ? xrow[kc] : make_uint4(0, 0, 0, 0), m < M);
+        return;
+    }
 #pragma unroll
     for (int h = 0; h < kXHeld; ++h) {
         const int kc = threadIdx.x + h * kXThreads;
@@ -621,8 +656,8 @@ cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16
     float *part = reinterpret_cast<float *>(ws + L.part_off);
     float *xscale = reinterpret_cast<float *>(ws + L.scale_off);
     unsigned int *cnt = reinterpret_cast<unsigned int *>(ws + L.cnt_off);
-    e = launch_pdl(x_tiles_kernel<TM>, dim3((unsigned)TM), dim3(kXThreads), 0, s, x, reinterpret_cast<uint4 *>(ws),
-                   xscale, (int)M, (int)K, cnt, S > 1 ? (int)tiles : 0);
+    e = launch_pdl(x_tiles_kernel<TM>, dim3((unsigned)TM), dim3(kXThreads), x_row_staged(K) ? (size_t)K * 2 : 0, s,
+                   x, reinterpret_cast<uint4 *>(ws), xscale, (int)M, (int)K, cnt, S > 1 ? (int)tiles : 0, err);
     if (e != cudaSuccess) return e;
     return launch_pdl(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads), C::kSmem, s,
                       reinterpret_cast<const uint4 *>(ws), wmap, y, part, cnt, static_cast<const float *>(xscale),
