@@ -164,13 +164,18 @@ __device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 u) {
 // what the epilogue multiplies the fp32 accumulator by (exact: a power of
 // two).  Values are written in the k order of the weight tiles (middle pair
 // of every group of four swapped).  One CTA per row: the row's maximum, then
-// the conversion of the chunks the threads still hold in registers (rows
-// longer than 6144 reload the rest).  Small in registers, so that its CTAs
-// fit beside the running GEMM's and start as soon as it completes.
+// the conversion of the chunks the threads still hold in registers (kHeld
+// 16-byte chunks a thread; longer rows reload the rest in each pass).  The
+// three-chunk form (K <= 6144) is small in registers, so that several CTAs
+// fit beside the running GEMM's and start as soon as it completes; rows of
+// 6144 < K <= 18432 take the nine-chunk form (64 registers, still one CTA
+// beside the GEMM): re-reading a thread's chunks beyond the third in both
+// passes had cost the K = 17408 pre-pass about 2 us more per call.
 constexpr int kXThreads = 256;
-constexpr int kXHeld = 3;  // chunks per thread kept in registers between the passes (K <= 6144)
-__global__ void __launch_bounds__(kXThreads, 8) x_to_f16_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x16,
-                                                              float *__restrict__ xscale, int kc8) {
+constexpr int kXHeldShort = 3, kXHeldLong = 9;  // chunks held a thread: K <= 6144, K <= 18432
+template <int kXHeld>
+__global__ void __launch_bounds__(kXThreads, kXHeld <= 3 ? 8 : 4)
+    x_to_f16_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x16, float *__restrict__ xscale, int kc8) {
     pdl_launch_dependents();
     pdl_wait();
     __shared__ uint32_t wmax[kXThreads / 32];
@@ -1114,9 +1119,10 @@ cudaError_t launch_gemm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf
     float *xscale = reinterpret_cast<float *>(ws + x16_bytes(M, K));
     float *part = reinterpret_cast<float *>(ws + x16_bytes(M, K) + xscale_bytes(M));
     if (!gemm_shape_supported(M, N, K)) return cudaErrorInvalidValue;
-    cudaError_t e = launch_pdl(x_to_f16_kernel, dim3((unsigned)M), dim3(kXThreads), 0, s,
-                               reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(x16), xscale,
-                               (int)(K / 8));
+    const bool long_rows = K > kXHeldShort * 8 * kXThreads && K <= kXHeldLong * 8 * kXThreads;
+    cudaError_t e = launch_pdl(long_rows ? x_to_f16_kernel<kXHeldLong> : x_to_f16_kernel<kXHeldShort>, dim3((unsigned)M),
+                               dim3(kXThreads), 0, s, reinterpret_cast<const uint4 *>(x),
+                               reinterpret_cast<uint4 *>(x16), xscale, (int)(K / 8));
     if (e != cudaSuccess) return e;
     int dev = 0;
     e = cudaGetDevice(&dev);
