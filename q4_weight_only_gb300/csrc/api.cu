@@ -18,6 +18,21 @@ __device__ unsigned int g_device_error_word;
 
 namespace {
 
+// x from page-locked host memory into the workspace, for the decode kernels
+// (M <= 2), whose every CTA reads all of x: read in place, a matmul of 152
+// CTAs pulled 152 copies of x over the host link, on the critical path after
+// its dependency wait.  Only the host writes x_host, so the loads go out
+// before this kernel's own dependency wait; the stores, into a workspace an
+// earlier kernel on the stream may still read, wait for it.
+__global__ void __launch_bounds__(256) stage_x_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                      int64_t n16) {
+    pdl_launch_dependents();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint4 v = i < n16 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+    pdl_wait();
+    if (i < n16) dst[i] = v;
+}
+
 // Self-check of the bounded-wait path: one thread waits on an mbarrier that
 // nothing arrives on, gives up after `limit_ns`, records the timeout in the
 // device error word and returns -- the same path every pipeline wait in this
@@ -393,8 +408,20 @@ int q4_0_matmul_host(const uint16_t *x_host, const uint8_t *wq, void *y_host, in
     const void *xdev = host_mapping(x_host), *ydev = host_mapping(y_host);
     if (xdev && ydev && aligned16(xdev) && aligned16(ydev)) {
         const size_t own = q4_0_matmul_workspace_bytes(M, N, K);
-        return matmul_ws_impl(static_cast<const uint16_t *>(xdev), wq, static_cast<float *>(const_cast<void *>(ydev)),
-                              bf16, M, N, K, own ? rest : nullptr, rest_bytes, stream);
+        const uint16_t *xk = static_cast<const uint16_t *>(xdev);
+        if (M <= 2) {
+            // the decode kernels read x in every CTA: one copy into the workspace first
+            const int st = check_matmul_args(xk, wq, static_cast<const float *>(ydev), M, N, K, true);
+            if (st != Q4_0_OK) return st;
+            const int64_t n16 = (int64_t)(xbytes / 16);
+            const cudaError_t e = launch_pdl(stage_x_kernel, dim3((unsigned)((n16 + 255) / 256)), dim3(256), 0,
+                                             static_cast<cudaStream_t>(stream), reinterpret_cast<const uint4 *>(xk),
+                                             reinterpret_cast<uint4 *>(xd), n16);
+            if (e != cudaSuccess) return Q4_0_ERR_CUDA;
+            xk = xd;
+        }
+        return matmul_ws_impl(xk, wq, static_cast<float *>(const_cast<void *>(ydev)), bf16, M, N, K,
+                              own ? rest : nullptr, rest_bytes, stream);
     }
     int st = check_matmul_args(xd, wq, yd, M, N, K, true);
     if (st != Q4_0_OK) return st;
