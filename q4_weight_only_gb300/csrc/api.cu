@@ -218,7 +218,7 @@ namespace {
 // The decode and GEMM paths with the output element type as a flag (the
 // public entry points below are these with fp32 y, or q4_0_matmul_ex).
 int gemv_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
-                 void *workspace, size_t workspace_bytes, void *stream) {
+                 void *workspace, size_t workspace_bytes, void *stream, bool x_host = false) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
     if (M > kGemvMaxM || !gemv_shape_supported(M, N, K)) return Q4_0_ERR_UNSUPPORTED;
@@ -228,7 +228,7 @@ int gemv_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int
     unsigned int *err = device_error_word();
     if (!err) return Q4_0_ERR_CUDA;
     return from_cuda(launch_gemv(x, wq, y, ybf16, M, N, K, need ? workspace : nullptr,
-                                 static_cast<cudaStream_t>(stream), err));
+                                 static_cast<cudaStream_t>(stream), err, x_host));
 }
 
 int gemm_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
@@ -248,8 +248,9 @@ int gemm_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_
         launch_gemm(x, wq, y, ybf16, M, N, K, workspace, splits, static_cast<cudaStream_t>(stream), err));
 }
 
+// x_host: x is page-locked host memory only the host writes (q4_0_matmul_host)
 int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
-                   void *workspace, size_t workspace_bytes, void *stream) {
+                   void *workspace, size_t workspace_bytes, void *stream, bool x_host = false) {
     int st = check_matmul_args(x, wq, y, M, N, K, true);
     if (st != Q4_0_OK) return st;
     const int64_t kk = K % 256 != 0 ? padded_k(K) : K;
@@ -272,7 +273,8 @@ int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, i
             return gemv_ws_impl(xp, wqp, y, ybf16, M, N, kp, rest_bytes ? rest : nullptr, rest_bytes, stream);
         return gemm_impl(xp, wqp, y, ybf16, M, N, kp, rest, rest_bytes, stream);
     }
-    if (M <= kDecodeMaxM) return gemv_ws_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
+    if (M <= kDecodeMaxM)
+        return gemv_ws_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream, x_host);
     return gemm_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
 }
 
@@ -421,7 +423,7 @@ int q4_0_matmul_host(const uint16_t *x_host, const uint8_t *wq, void *y_host, in
             xk = xd;
         }
         return matmul_ws_impl(xk, wq, static_cast<float *>(const_cast<void *>(ydev)), bf16, M, N, K,
-                              own ? rest : nullptr, rest_bytes, stream);
+                              own ? rest : nullptr, rest_bytes, stream, /*x_host=*/xk != xd);
     }
     int st = check_matmul_args(xd, wq, yd, M, N, K, true);
     if (st != Q4_0_OK) return st;
