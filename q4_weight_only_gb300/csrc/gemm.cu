@@ -1040,7 +1040,9 @@ int64_t xscale_bytes(int64_t M) { return (M * 4 + 255) / 256 * 256; }
 // Rows of x per CTA tile.  Each extra tile dequantises every weight tile
 // once more, but tiles of more than 256 rows run with a shallower x ring:
 // they are used when they need at most three quarters as many tiles as
-// 256-row ones (M = 272: one tile instead of two).  From four 256-row
+// 256-row ones (M = 272: one tile instead of two).  When two or more
+// 256-row tiles leave SMs idle in a single wave, more, shorter tiles fill it
+// (see below).  From four 256-row
 // tiles up (M > 768), when both tilings give every SM at least one tile (so
 // K is not split) and `sms` is known, whole waves decide instead: a wave
 // costs its tile height plus about 100 rows'
@@ -1054,6 +1056,14 @@ int tile_rows(int64_t M, int64_t N, int sms) {
     const int64_t t256 = (M + 255) / 256, tall = (M + kMaxTileRows - 1) / kMaxTileRows;
     int64_t tiles_m = 4 * tall <= 3 * t256 ? tall : t256;
     const int64_t nt = (N + kTileN - 1) / kTileN;
+    // two or more 256-row tiles in one partial wave (SMs left idle): the most
+    // x tiles, of at least 144 rows, that still fit one wave (the O and down
+    // projections at M = 512: three tiles of 176 rows, 120 of 152 SMs busy
+    // instead of 80)
+    if (sms > 0 && tiles_m == t256 && t256 >= 2 && t256 * nt < sms) {
+        for (int64_t c = t256 + 1; c * nt <= sms && ((M + c - 1) / c + 15) / 16 * 16 >= 144; ++c) tiles_m = c;
+        return (int)(((M + tiles_m - 1) / tiles_m + 15) / 16 * 16);
+    }
     if (sms > 0 && t256 >= 4 && tall < t256 && tall * nt >= sms) {
         auto cost = [&](int64_t tm_count) {
             const int64_t rows = ((M + tm_count - 1) / tm_count + 15) / 16 * 16;

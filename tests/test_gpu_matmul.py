@@ -359,8 +359,11 @@ def test_matmul_host_equals_device_call():
     gives: with page-locked buffers (read and written by the kernels in
     place) and with pageable ones (copied in and out)."""
     q4 = lib()
+    # M <= 2: x staged into the workspace by a copy kernel; 3 <= M <= 64: the
+    # batched decode's pre-pass reads host x before its dependency wait
+    # (K = 9216 and 17408: rows staged in shared memory by bulk copies)
     for M, N, K in ((1, 1000, 5120), (2, 300, 1024), (16, 300, 2048), (64, 260, 1024), (300, 200, 512),
-                    (1, 100, 96)):
+                    (1, 100, 96), (3, 200, 9216), (16, 256, 17408)):
         x, wq = case(8400 + M, M, N, K)
         wd = wq_dev(wq)
         x_pageable = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16)
@@ -480,6 +483,10 @@ def test_gemm_plan():
         for K in (5120, 17408):
             p = q4.gemm_plan(2048, 5120, K)
             assert p == {"tile_rows": 304, "splits": 1, "persistent": True}, p
+            # M = 512: two 256-row tiles leave SMs idle in one wave; three of
+            # 176 rows fill 120 of 152
+            p = q4.gemm_plan(512, 5120, K)
+            assert p == {"tile_rows": 176, "splits": 1, "persistent": False}, p
     p = q4.gemm_plan(272, 34816, 5120)
     assert p == {"tile_rows": 272, "splits": 1, "persistent": True}
     assert not q4.gemm_plan(96, 5120, 5120)["persistent"]
@@ -502,6 +509,21 @@ def test_gemm_wave_aware_tall_tiles_every_output():
     check_full(y, x, wq, N, K)
     assert torch.equal(q4.gemm(xd, wd, N, K), y)
     assert torch.equal(q4.matmul(xd, wd, N, K), y)
+    assert q4.device_error() == 0
+
+
+def test_gemm_one_wave_short_tiles_every_output():
+    """M = 512 against 40 weight tiles takes three x tiles of 176 rows (the
+    last ragged, 160 rows) in one wave: every output against the oracle,
+    with fp32 and bf16 y."""
+    q4 = lib()
+    M, N, K = 512, 5120, 1024
+    assert q4.gemm_plan(M, N, K)["tile_rows"] < 256
+    x, wq = case(9910, M, N, K, act_outliers=0.01)
+    xd, wd = x_dev(x), wq_dev(wq)
+    y = q4.matmul(xd, wd, N, K)
+    check_full(y, x, wq, N, K)
+    assert torch.equal(q4.matmul(xd, wd, N, K, out_dtype=torch.bfloat16), y.to(torch.bfloat16))
     assert q4.device_error() == 0
 
 
