@@ -201,11 +201,15 @@ int q4_0_matmul_ex(const uint16_t *x, const uint8_t *wq, void *y, int y_type,
  * `stream` in that order.  wq is the device Q4_0 matrix as for q4_0_matmul.
  * When both host buffers are page-locked memory the device can address
  * (cudaHostAlloc / cudaHostRegister; on a GB300 the Grace memory is coherent
- * with the GPU over NVLink-C2C) and 16-byte aligned there, the kernels read
- * x and write y in host memory directly and no copy is issued; otherwise x
- * and y are copied with plain cudaMemcpyAsync (page-locked buffers let the
- * copies overlap the host).  Either way the caller synchronises `stream`
- * before reading y (or reusing x).
+ * with the GPU over NVLink-C2C) and 16-byte aligned there, the kernels
+ * write y in host memory directly and no copy is issued: for M <= 2 a small
+ * kernel first copies x into the workspace (the decode kernels read all of
+ * x in every CTA; its loads are issued before it waits for the previous
+ * kernel on the stream, so the host must not change x until the stream has
+ * passed this call), and larger M read x in host memory where they convert
+ * it.  Otherwise x and y are copied with plain cudaMemcpyAsync (page-locked
+ * buffers let the copies overlap the host).  Either way the caller
+ * synchronises `stream` before reading y (or reusing x).
  * Workspace: device memory, 16-byte aligned, of at least
  * q4_0_matmul_host_workspace_bytes(M, N, K, y_type) bytes: the device copies
  * of x and y (each rounded up to 256 bytes) and the matmul's own scratch;
