@@ -204,10 +204,10 @@ int q4_0_matmul_ex(const uint16_t *x, const uint8_t *wq, void *y, int y_type,
  * with the GPU over NVLink-C2C) and 16-byte aligned there, the kernels
  * write y in host memory directly and no copy is issued: for M <= 2 a small
  * kernel first copies x into the workspace (the decode kernels read all of
- * x in every CTA; its loads are issued before it waits for the previous
- * kernel on the stream, so the host must not change x until the stream has
- * passed this call), and larger M read x in host memory where they convert
- * it.  Otherwise x and y are copied with plain cudaMemcpyAsync (page-locked
+ * x in every CTA), and larger M read x in host memory where they convert
+ * it; either way x is read in stream order, so y of an earlier call on the
+ * stream may be passed as x.  Otherwise x and y are copied with plain
+ * cudaMemcpyAsync (page-locked
  * buffers let the copies overlap the host).  Either way the caller
  * synchronises `stream` before reading y (or reusing x).
  * Workspace: device memory, 16-byte aligned, of at least

@@ -21,16 +21,15 @@ namespace {
 // x from page-locked host memory into the workspace, for the decode kernels
 // (M <= 2), whose every CTA reads all of x: read in place, a matmul of 152
 // CTAs pulled 152 copies of x over the host link, on the critical path after
-// its dependency wait.  Only the host writes x_host, so the loads go out
-// before this kernel's own dependency wait; the stores, into a workspace an
-// earlier kernel on the stream may still read, wait for it.
+// its dependency wait.  x is read only after this kernel's own dependency
+// wait: an earlier kernel on the stream may write it (y of an earlier call
+// passed as x), and this library's kernels let their dependents start early.
 __global__ void __launch_bounds__(256) stage_x_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                                       int64_t n16) {
     pdl_launch_dependents();
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const uint4 v = i < n16 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
     pdl_wait();
-    if (i < n16) dst[i] = v;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n16) dst[i] = src[i];
 }
 
 // Self-check of the bounded-wait path: one thread waits on an mbarrier that
@@ -218,7 +217,7 @@ namespace {
 // The decode and GEMM paths with the output element type as a flag (the
 // public entry points below are these with fp32 y, or q4_0_matmul_ex).
 int gemv_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
-                 void *workspace, size_t workspace_bytes, void *stream, bool x_host = false) {
+                 void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K);
     if (st != Q4_0_OK) return st;
     if (M > kGemvMaxM || !gemv_shape_supported(M, N, K)) return Q4_0_ERR_UNSUPPORTED;
@@ -228,7 +227,7 @@ int gemv_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int
     unsigned int *err = device_error_word();
     if (!err) return Q4_0_ERR_CUDA;
     return from_cuda(launch_gemv(x, wq, y, ybf16, M, N, K, need ? workspace : nullptr,
-                                 static_cast<cudaStream_t>(stream), err, x_host));
+                                 static_cast<cudaStream_t>(stream), err));
 }
 
 int gemm_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
@@ -248,9 +247,8 @@ int gemm_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_
         launch_gemm(x, wq, y, ybf16, M, N, K, workspace, splits, static_cast<cudaStream_t>(stream), err));
 }
 
-// x_host: x is page-locked host memory only the host writes (q4_0_matmul_host)
 int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N, int64_t K,
-                   void *workspace, size_t workspace_bytes, void *stream, bool x_host = false) {
+                   void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_matmul_args(x, wq, y, M, N, K, true);
     if (st != Q4_0_OK) return st;
     const int64_t kk = K % 256 != 0 ? padded_k(K) : K;
@@ -273,8 +271,7 @@ int matmul_ws_impl(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, i
             return gemv_ws_impl(xp, wqp, y, ybf16, M, N, kp, rest_bytes ? rest : nullptr, rest_bytes, stream);
         return gemm_impl(xp, wqp, y, ybf16, M, N, kp, rest, rest_bytes, stream);
     }
-    if (M <= kDecodeMaxM)
-        return gemv_ws_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream, x_host);
+    if (M <= kDecodeMaxM) return gemv_ws_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
     return gemm_impl(x, wq, y, ybf16, M, N, K, workspace, workspace_bytes, stream);
 }
 
@@ -423,7 +420,7 @@ int q4_0_matmul_host(const uint16_t *x_host, const uint8_t *wq, void *y_host, in
             xk = xd;
         }
         return matmul_ws_impl(xk, wq, static_cast<float *>(const_cast<void *>(ydev)), bf16, M, N, K,
-                              own ? rest : nullptr, rest_bytes, stream, /*x_host=*/xk != xd);
+                              own ? rest : nullptr, rest_bytes, stream);
     }
     int st = check_matmul_args(xd, wq, yd, M, N, K, true);
     if (st != Q4_0_OK) return st;

@@ -1142,10 +1142,10 @@ cudaError_t launch_gemv_grouped(int G, const uint16_t *const *x, const uint8_t *
 }
 
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
-                        int64_t K, void *workspace, cudaStream_t s, unsigned int *err, bool x_host) {
+                        int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
     // three or more rows of x (or a K too long to hold in shared memory): the
     // dot product moves to the tensor cores
-    if (decode_on_tensor_cores(M, K)) return launch_gemv_tc(x, wq, y, ybf16, M, N, K, workspace, s, err, x_host);
+    if (decode_on_tensor_cores(M, K)) return launch_gemv_tc(x, wq, y, ybf16, M, N, K, workspace, s, err);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -166,10 +166,7 @@ constexpr int kXThreads = 128;
 constexpr int kXHeld = 8;  // chunks per thread kept in registers between the passes (K <= 8192)
 constexpr int kXStagedMaxK = 24576;  // rows staged in shared memory: K * 2 bytes <= 48 KB
 __host__ __device__ constexpr bool x_row_staged(int64_t K) { return K > kXHeld * 8 * kXThreads && K <= kXStagedMaxK; }
-// kXHost: x is host memory that only the host writes, so the row is read
-// before the dependency wait (its stores into the workspace still wait); a
-// separate instantiation keeps the device-memory form unchanged.
-template <int TM, bool kXHost>
+template <int TM>
 __global__ void __launch_bounds__(kXThreads, 9) x_tiles_kernel(const uint16_t *__restrict__ x, uint4 *__restrict__ xt,
                                                             float *__restrict__ xscale, int M, int K,
                                                             unsigned int *__restrict__ tile_cnt, int ncnt,
@@ -187,37 +184,24 @@ __global__ void __launch_bounds__(kXThreads, 9) x_tiles_kernel(const uint16_t *_
         xabort = 0;
         mbar_fence_init();
     }
-    // the row into shared memory (staged rows): before the dependency wait
-    // when only the host writes x
-    auto stage_row = [&]() {
-        if (staged && threadIdx.x == 0 && m < M) {
-            const uint32_t bytes = (uint32_t)K * 2;
-            mbar_arrive_expect_tx(&xbar, bytes);
-            for (uint32_t off = 0; off < bytes; off += 16384)
-                bulk_g2s(reinterpret_cast<uint8_t *>(xrow) + off, reinterpret_cast<const uint8_t *>(src) + off,
-                         bytes - off < 16384 ? bytes - off : 16384, &xbar);
-        }
-    };
-    if constexpr (kXHost) stage_row();
-    uint4 held[kXHeld];
-#pragma unroll
-    for (int h = 0; h < kXHeld; ++h) held[h] = make_uint4(0, 0, 0, 0);
-    if (kXHost && !staged && m < M) {
-#pragma unroll
-        for (int h = 0; h < kXHeld; ++h) {
-            const int kc = threadIdx.x + h * kXThreads;
-            if (kc < kc8) held[h] = __ldg(src + kc);
-        }
-    }
     pdl_wait();  // x may come from the previous kernel (and the last one has read its counters)
     if (blockIdx.x == 0)  // the split-K tile counters of the matmul kernel that follows
         for (int i = threadIdx.x; i < ncnt; i += kXThreads) tile_cnt[i] = 0u;
     __shared__ uint32_t wmax[kXThreads / 32];
+    uint4 held[kXHeld];
+#pragma unroll
+    for (int h = 0; h < kXHeld; ++h) held[h] = make_uint4(0, 0, 0, 0);
     uint32_t mb = 0;
     if (staged) {
         __syncthreads();  // the barrier's initialisation
         if (m < M) {
-            if (!kXHost) stage_row();
+            if (threadIdx.x == 0) {
+                const uint32_t bytes = (uint32_t)K * 2;
+                mbar_arrive_expect_tx(&xbar, bytes);
+                for (uint32_t off = 0; off < bytes; off += 16384)
+                    bulk_g2s(reinterpret_cast<uint8_t *>(xrow) + off, reinterpret_cast<const uint8_t *>(src) + off,
+                             bytes - off < 16384 ? bytes - off : 16384, &xbar);
+            }
             const bool ok = mbar_wait(&xbar, 0, &xabort, err);
             for (int kc = threadIdx.x; ok && kc < kc8; kc += kXThreads) mb = max(mb, bf16x8_absmax_bits(xrow[kc]));
             if (!ok) mbar_drain(&xbar, 0);  // the copies land before the CTA can exit
@@ -227,7 +211,7 @@ __global__ void __launch_bounds__(kXThreads, 9) x_tiles_kernel(const uint16_t *_
         for (int h = 0; h < kXHeld; ++h) {
             const int kc = threadIdx.x + h * kXThreads;
             if (kc < kc8) {
-                if (!kXHost) held[h] = __ldg(src + kc);
+                held[h] = __ldg(src + kc);
                 mb = max(mb, bf16x8_absmax_bits(held[h]));
             }
         }
@@ -637,7 +621,7 @@ struct WorkspaceLayout {
 
 template <int TM>
 cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
-                      int64_t K, void *workspace, cudaStream_t s, unsigned int *err, bool x_host) {
+                      int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
     using C = Cfg<TM>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -672,9 +656,8 @@ cudaError_t launch_tm(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16
     float *part = reinterpret_cast<float *>(ws + L.part_off);
     float *xscale = reinterpret_cast<float *>(ws + L.scale_off);
     unsigned int *cnt = reinterpret_cast<unsigned int *>(ws + L.cnt_off);
-    e = launch_pdl(x_host ? x_tiles_kernel<TM, true> : x_tiles_kernel<TM, false>, dim3((unsigned)TM),
-                   dim3(kXThreads), x_row_staged(K) ? (size_t)K * 2 : 0, s, x, reinterpret_cast<uint4 *>(ws), xscale,
-                   (int)M, (int)K, cnt, S > 1 ? (int)tiles : 0, err);
+    e = launch_pdl(x_tiles_kernel<TM>, dim3((unsigned)TM), dim3(kXThreads), x_row_staged(K) ? (size_t)K * 2 : 0, s,
+                   x, reinterpret_cast<uint4 *>(ws), xscale, (int)M, (int)K, cnt, S > 1 ? (int)tiles : 0, err);
     if (e != cudaSuccess) return e;
     return launch_pdl(gemv_tc_kernel<TM>, dim3((unsigned)S, (unsigned)tiles), dim3(kThreads), C::kSmem, s,
                       reinterpret_cast<const uint4 *>(ws), wmap, y, part, cnt, static_cast<const float *>(xscale),
@@ -695,11 +678,11 @@ size_t gemv_tc_workspace_bytes(int64_t M, int64_t K) {
 }
 
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
-                           int64_t K, void *workspace, cudaStream_t s, unsigned int *err, bool x_host) {
+                           int64_t K, void *workspace, cudaStream_t s, unsigned int *err) {
     switch (tile_rows_tc(M)) {
-        case 16: return launch_tm<16>(x, wq, y, ybf16, M, N, K, workspace, s, err, x_host);
-        case 32: return launch_tm<32>(x, wq, y, ybf16, M, N, K, workspace, s, err, x_host);
-        default: return launch_tm<64>(x, wq, y, ybf16, M, N, K, workspace, s, err, x_host);
+        case 16: return launch_tm<16>(x, wq, y, ybf16, M, N, K, workspace, s, err);
+        case 32: return launch_tm<32>(x, wq, y, ybf16, M, N, K, workspace, s, err);
+        default: return launch_tm<64>(x, wq, y, ybf16, M, N, K, workspace, s, err);
     }
 }
 

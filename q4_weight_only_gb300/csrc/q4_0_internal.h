@@ -74,17 +74,15 @@ int grouped_decode_launches(int G, int64_t M, const int64_t *N, const int64_t *K
 cudaError_t launch_gemv_grouped(int G, const uint16_t *const *x, const uint8_t *const *wq, float *const *y,
                                 bool ybf16, int64_t M, const int64_t *N, const int64_t *K, cudaStream_t s,
                                 unsigned int *err);
-// x_host: x is page-locked host memory that only the host writes, so the
-// tensor-core decode's x pre-pass may read it before its dependency wait.
 cudaError_t launch_gemv(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
-                        int64_t K, void *workspace, cudaStream_t s, unsigned int *err, bool x_host = false);
+                        int64_t K, void *workspace, cudaStream_t s, unsigned int *err);
 
 // Tensor-core decode for M <= 64: x rounded once into binary16 MMA tiles in
 // the workspace (gemv_tc_workspace_bytes(M, K) bytes, which also holds the
 // split-K partial tiles and counters).  N <= 65535 * 128.
 size_t gemv_tc_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_gemv_tc(const uint16_t *x, const uint8_t *wq, float *y, bool ybf16, int64_t M, int64_t N,
-                           int64_t K, void *xtiles, cudaStream_t s, unsigned int *err, bool x_host = false);
+                           int64_t K, void *xtiles, cudaStream_t s, unsigned int *err);
 
 // K % 32 == 0 but K % 256 != 0: W and x copied, zero-padded to K rounded up
 // to 256 (padded_k), into the front of `workspace` (pad_bytes(M, N, K)

@@ -379,6 +379,32 @@ def test_matmul_host_equals_device_call():
                 assert torch.equal(y, ref), (M, N, K, dt, pinned)
 
 
+def test_matmul_host_chained_through_host_memory():
+    """y of one q4_0_matmul_host call (bf16, page-locked) passed as x of the
+    next on the same stream, with no synchronisation between them: the second
+    call reads x in stream order, so both match the same chain on device
+    buffers bit for bit (M = 1 copies x into the workspace first; M = 16
+    reads it in its x pre-pass)."""
+    q4 = lib()
+    K0, N0, N1 = 1024, 1024, 512
+    for M in (1, 16):
+        x, wq0 = case(8500 + M, M, N0, K0)
+        _, wq1 = case(8600 + M, M, N1, N0)
+        wd0, wd1 = wq_dev(wq0), wq_dev(wq1)
+        xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+        st = torch.cuda.current_stream()
+        for rep in range(3):
+            y0 = torch.full((M, N0), float("nan"), dtype=torch.bfloat16, pin_memory=True)
+            y1 = torch.empty((M, N1), dtype=torch.float32, pin_memory=True)
+            q4.matmul_host(xh, wd0, N0, K0, out=y0, out_dtype=torch.bfloat16, stream=st)
+            q4.matmul_host(y0, wd1, N1, N0, out=y1, stream=st)
+            st.synchronize()
+            r0 = q4.matmul(xh.cuda(), wd0, N0, K0, out_dtype=torch.bfloat16)
+            r1 = q4.matmul(r0, wd1, N1, N0).cpu()
+            assert torch.equal(y0, r0.cpu()), (M, rep)
+            assert torch.equal(y1, r1), (M, rep)
+
+
 def test_graph_capture_replays_bitwise():
     """A decode step captured into a CUDA graph (decode, batched decode and
     GEMM calls back to back under programmatic dependent launch, each with
