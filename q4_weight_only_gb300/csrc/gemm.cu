@@ -1040,26 +1040,25 @@ int64_t xscale_bytes(int64_t M) { return (M * 4 + 255) / 256 * 256; }
 // Rows of x per CTA tile.  Each extra tile dequantises every weight tile
 // once more, but tiles of more than 256 rows run with a shallower x ring:
 // they are used when they need at most three quarters as many tiles as
-// 256-row ones (M = 272: one tile instead of two).  When two or more
-// 256-row tiles leave SMs idle in a single wave, more, shorter tiles fill it
-// (see below).  From four 256-row
-// tiles up (M > 768), when both tilings give every SM at least one tile (so
-// K is not split) and `sms` is known, whole waves decide instead: a wave
-// costs its tile height plus about 100 rows'
-// worth of MMA time for the tile's own work (its weight tile's
-// dequantisation, the epilogue), and tall tiles are taken when that saves
-// more than 5 % (the O and down projections at M = 2048: seven tiles of 304
-// rows, 280 tiles on 152 SMs in two waves, instead of eight of 256, 320
-// tiles in three).  Then the smallest multiple of 16 that covers M in that
-// many tiles.
+// 256-row ones (M = 272: one tile instead of two).  With `sms` known, two
+// further rules look at waves of tiles (one CTA per SM):
+//   * two or more 256-row tiles that leave SMs idle in a single wave: the
+//     most x tiles of at least 144 rows that still fit one wave (the O and
+//     down projections at M = 512: three tiles of 176 rows, 120 of 152 SMs
+//     busy instead of 80);
+//   * from four 256-row tiles up (M > 768), when both tilings give every SM
+//     at least one tile (so K is not split): the tiling whose whole waves
+//     cost less, a wave costing its tile height plus about 100 rows' worth
+//     of MMA time for the tile's own work (its weight tile's
+//     dequantisation, the epilogue); tall tiles are taken when that saves
+//     more than 5 % (O and down at M = 2048: seven tiles of 304 rows, 280
+//     tiles in two waves on 152 SMs, instead of eight of 256, 320 tiles in
+//     three).
+// Then the smallest multiple of 16 that covers M in that many tiles.
 int tile_rows(int64_t M, int64_t N, int sms) {
     const int64_t t256 = (M + 255) / 256, tall = (M + kMaxTileRows - 1) / kMaxTileRows;
     int64_t tiles_m = 4 * tall <= 3 * t256 ? tall : t256;
     const int64_t nt = (N + kTileN - 1) / kTileN;
-    // two or more 256-row tiles in one partial wave (SMs left idle): the most
-    // x tiles, of at least 144 rows, that still fit one wave (the O and down
-    // projections at M = 512: three tiles of 176 rows, 120 of 152 SMs busy
-    // instead of 80)
     if (sms > 0 && tiles_m == t256 && t256 >= 2 && t256 * nt < sms) {
         for (int64_t c = t256 + 1; c * nt <= sms && ((M + c - 1) / c + 15) / 16 * 16 >= 144; ++c) tiles_m = c;
         return (int)(((M + tiles_m - 1) / tiles_m + 15) / 16 * 16);
