@@ -157,11 +157,12 @@ __device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 u) {
 // conversion of the chunks the threads still hold in registers.  Rows of
 // 8192 < K <= 24576 are first brought into shared memory by bulk copies
 // (one round trip; with a thread's chunks beyond the eight it holds
-// re-read from L2 in each pass, the K = 17408 pre-pass had cost about 2 us
-// more per call); longer rows reload the rest.  128 threads of at most 56
-// registers (and at most 48 KB of shared memory), so that its CTAs fit
-// beside two CTAs of the running decode kernel and start as soon as it
-// completes.
+// re-read from L2 in each pass, the down projection, K = 17408, took about
+// 1 us longer per call); longer rows reload the rest.  128 threads of at
+// most 56 registers, so that its CTAs fit beside two CTAs of the running
+// decode kernel and start as soon as it completes (a staged row's 48 KB of
+// shared memory at most still fits beside those of 16- and 32-row tiles,
+// not beside 64-row ones).
 constexpr int kXThreads = 128;
 constexpr int kXHeld = 8;  // chunks per thread kept in registers between the passes (K <= 8192)
 constexpr int kXStagedMaxK = 24576;  // rows staged in shared memory: K * 2 bytes <= 48 KB
