@@ -170,7 +170,8 @@ __device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 u) {
 // fit beside the running GEMM's and start as soon as it completes; rows of
 // 6144 < K <= 18432 take the nine-chunk form (64 registers, still one CTA
 // beside the GEMM): re-reading a thread's chunks beyond the third in both
-// passes had cost the K = 17408 pre-pass about 2 us more per call.
+// passes had made the down projection (K = 17408) 2.4 us (M = 2048) to
+// 3 us (M = 272) slower per call.
 constexpr int kXThreads = 256;
 constexpr int kXHeldShort = 3, kXHeldLong = 9;  // chunks held a thread: K <= 6144, K <= 18432
 template <int kXHeld>
