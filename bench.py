@@ -354,10 +354,7 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
     parts_t = {"api": 0.0, "sync": 0.0, "device": 0.0}
     ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    def e2e_step(i, account=False):
-        t_a = time.perf_counter()
-        if account:
-            ev_a.record(stream)
+    def issue(i):
         ls = range(layers) if sweep else (i % layers,)
         for l in ls:
             if grouped:
@@ -373,6 +370,12 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
                 for p in range(len(parts)):
                     q4.matmul_host(x_views[j][p], wq[l][j], N, K, out=y_views[j][p], workspace=whs[j][p],
                                    stream=stream, out_dtype=ydt)
+
+    def e2e_step(i, account=False):
+        t_a = time.perf_counter()
+        if account:
+            ev_a.record(stream)
+        issue(i)
         if account:
             ev_b.record(stream)
         t_b = time.perf_counter()
@@ -398,9 +401,32 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
     with torch.cuda.stream(stream):
         for i in range(acc_steps):
             e2e_step(i, account=True)
+    # the same calls captured once per layer copy (per step of the sweep) as
+    # CUDA graphs, one replay and one wait per step: the step of a server that
+    # replays its calls as a graph, host copies still inside every step
+    n_gr = 1 if sweep else layers
+    graphs = []
+    for i in range(n_gr):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            issue(i)
+        graphs.append(gr)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, n_gr)):  # every graph replays once (its upload) before the timing
+            graphs[i % n_gr].replay()
+            stream.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            graphs[i % n_gr].replay()
+            stream.synchronize()
+    t_graph = max_over_ranks(time.perf_counter() - t0, world)
+    del graphs, gr
     barrier(world)
     tensor_bound = M >= 256
     e2e_val = (step_flops if tensor_bound else step_bytes) * e2e_steps * world / t_e2e / (1e12 if tensor_bound else 1e9)
+    graph_val = e2e_val * t_e2e / t_graph
 
     unit = "TFLOP/s" if tensor_bound else "GB/s"
     value = tflops if tensor_bound else gbs
@@ -440,7 +466,12 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
                        "steps": acc_steps,
                        "host_in_library_calls": round(parts_t["api"] / acc_steps * 1e6, 2),
                        "waiting_for_the_step": round(parts_t["sync"] / acc_steps * 1e6, 2),
-                       "device_time_of_the_step": round(parts_t["device"] / acc_steps * 1e6, 2)}},
+                       "device_time_of_the_step": round(parts_t["device"] / acc_steps * 1e6, 2)},
+                   "graph_replay": {
+                       "value": round(graph_val, 2), "us_per_step": round(t_graph / e2e_steps * 1e6, 2),
+                       "steps": e2e_steps,
+                       "how": "the step's library calls captured once per layer copy as CUDA graphs; "
+                              "one replay and one stream wait per step"}},
            "layer_copies": layers,
            "graphs": " + ".join(f"{reps} x {n} steps" for _, n, reps in plan)}
     if cpu:
