@@ -404,29 +404,33 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
     # the same calls captured once per layer copy (per step of the sweep) as
     # CUDA graphs, one replay and one wait per step: the step of a server that
     # replays its calls as a graph, host copies still inside every step
-    n_gr = 1 if sweep else layers
-    graphs = []
-    for i in range(n_gr):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=stream):
-            issue(i)
-        graphs.append(gr)
-    with torch.cuda.stream(stream):
-        for i in range(max(3, n_gr)):  # every graph replays once (its upload) before the timing
-            graphs[i % n_gr].replay()
-            stream.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(e2e_steps):
-            graphs[i % n_gr].replay()
-            stream.synchronize()
-    t_graph = max_over_ranks(time.perf_counter() - t0, world)
-    del graphs, gr
+    # (the grouped form's e2e copies x and y with torch around its call and
+    # is timed with direct calls only)
+    t_graph = None
+    if not grouped:
+        n_gr = 1 if sweep else layers
+        graphs = []
+        for i in range(n_gr):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                issue(i)
+            graphs.append(gr)
+        with torch.cuda.stream(stream):
+            for i in range(max(3, n_gr)):  # every graph replays once (its upload) before the timing
+                graphs[i % n_gr].replay()
+                stream.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(e2e_steps):
+                graphs[i % n_gr].replay()
+                stream.synchronize()
+        t_graph = max_over_ranks(time.perf_counter() - t0, world)
+        del graphs, gr
     barrier(world)
     tensor_bound = M >= 256
     e2e_val = (step_flops if tensor_bound else step_bytes) * e2e_steps * world / t_e2e / (1e12 if tensor_bound else 1e9)
-    graph_val = e2e_val * t_e2e / t_graph
+    graph_val = e2e_val * t_e2e / t_graph if t_graph else None
 
     unit = "TFLOP/s" if tensor_bound else "GB/s"
     value = tflops if tensor_bound else gbs
@@ -451,7 +455,10 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
                 "flops_per_launch": round(step_flops / calls_per_step),
                 "avg_launch_us": round(ms_local * 1e3 / calls, 3),
                 "timing": "whole step on the launching stream (x pre-pass and split-K sum included), / matmul calls"}
-    traffic = load_traffic("grouped" if grouped else workload, M)
+    # the sweep runs the decode (M = 1) or batched (M = 16) step's four
+    # shapes through the same kernels, every layer's weights cold in L2 as
+    # in those steps: the same bytes per launch
+    traffic = load_traffic("grouped" if grouped else ("decode" if M == 1 else "batched") if sweep else workload, M)
     if traffic is not None:
         roof["traffic"] = traffic
     res = {"workload": workload_name(workload, M, layers, grouped), "M": M,
@@ -467,7 +474,7 @@ def measure(q4, synth, wq, workload, M, args, dev, world, grouped=False, cpu=Fal
                        "host_in_library_calls": round(parts_t["api"] / acc_steps * 1e6, 2),
                        "waiting_for_the_step": round(parts_t["sync"] / acc_steps * 1e6, 2),
                        "device_time_of_the_step": round(parts_t["device"] / acc_steps * 1e6, 2)},
-                   "graph_replay": {
+                   "graph_replay": None if t_graph is None else {
                        "value": round(graph_val, 2), "us_per_step": round(t_graph / e2e_steps * 1e6, 2),
                        "steps": e2e_steps,
                        "how": "the step's library calls captured once per layer copy as CUDA graphs; "

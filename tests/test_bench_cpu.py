@@ -75,3 +75,16 @@ def test_reference_arm_two_ranks_rank0_alone_prints():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0
+
+
+def test_traffic_lookup_follows_the_kernel_source():
+    """profiles/traffic.json resolves for every workload whose kernel source
+    is unchanged since its capture, and only for the M it was captured at."""
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        table = json.load(f)
+    for name, entry in table.items():
+        assert bench.load_traffic(name, entry["M"]) == entry["bytes_per_launch"], name
+        assert bench.load_traffic(name, entry["M"] + 1) is None
+    assert bench.load_traffic("no such workload", 1) is None
